@@ -1,0 +1,254 @@
+"""Python binding of libbqgemv (block-quantized skinny GEMV for sm_103a).
+
+A thin ctypes layer over the C ABI in include/bqgemv.h: every function here
+has the name of its C entry point without the ``bqg_`` prefix, checks that
+the torch tensors it is given match the C contract, and passes raw device
+pointers plus the current CUDA stream.  All arithmetic runs in the library's
+CUDA kernels; PyTorch only provides device memory and streams.  There is no
+fallback: if the shared library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+BF16, Q8_0, Q4_0, Q8_1, F32 = 0, 1, 2, 3, 4
+OP_GEMV_BF16, OP_GEMV_Q8_0, OP_GEMV_Q4_0, OP_GEMV_Q4_0_Q8_1 = 0, 1, 2, 3
+OP_QKV_Q4_0_Q8_1, OP_GATE_UP_Q4_0_Q8_1, OP_GEMM_Q4_0_BF16 = 4, 5, 6
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q8_1: 36}
+QK = 32
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libbqgemv.so")
+
+EXPORTS = {
+    # name: (argtypes, restype)
+    "bqg_repacked_size": (["i", "i64", "i64"], "size"),
+    "bqg_quantize_weights": (["i", "p", "p", "i64", "i64", "p"], "i"),
+    "bqg_repack_weights": (["i", "p", "p", "i64", "i64", "p"], "i"),
+    "bqg_quantize_q8_1": (["p", "i", "p", "i", "i64", "p"], "i"),
+    "bqg_gemv_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_gemv_q8_0": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_gemv_q4_0": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_gemv_q4_0_q8_1": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_gemv_q4_0_q8_1_qkv": (["p", "p", "p", "p", "p", "p", "p", "i", "i64", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_gemv_q4_0_q8_1_gate_up_swiglu": (["p", "p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_gemm_q4_0_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_debug_q4_0_q8_1_block_dots": (["p", "p", "p", "i64", "i64", "p"], "i"),
+    "bqg_workspace_size": (["i", "i", "i64", "i64"], "size"),
+    "bqg_last_device_error": (["p", "p"], "i"),
+    "bqg_set_pdl": (["i"], "i"),
+    "bqg_status_string": (["i"], "str"),
+    "bqg_version": ([], "str"),
+}
+_CT = {"i": ctypes.c_int, "i64": ctypes.c_int64, "p": ctypes.c_void_p, "size": ctypes.c_size_t,
+       "str": ctypes.c_char_p}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class BqgError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (once) and return the shared library; raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libbqgemv is not built ({p} missing); run "
+                                   "block_quantized_gemv_gb300.build.build()")
+            L = ctypes.CDLL(p)
+            for name, (args, res) in EXPORTS.items():
+                fn = getattr(L, name)
+                fn.argtypes = [_CT[a] for a in args]
+                fn.restype = _CT[res]
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().bqg_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return load().bqg_version().decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise BqgError(status, where)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, numel=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() * t.element_size() < numel:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, needs {numel}")
+    return t.data_ptr()
+
+
+def _ws(ws):
+    if ws is None:
+        return None, 0
+    _dev(ws, "ws")
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+def row_bytes(fmt: int, K: int) -> int:
+    """Bytes of one canonical row (bf16: 2K; block formats: K/32 blocks)."""
+    return 2 * K if fmt == BF16 else (K // QK) * BLOCK_BYTES[fmt]
+
+
+# --- load time -----------------------------------------------------------------
+def repacked_size(fmt: int, N: int, K: int) -> int:
+    return int(load().bqg_repacked_size(fmt, N, K))
+
+
+def quantize_weights(fmt: int, W: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 N x K -> canonical q8_0/q4_0 blocks (uint8, N x row_bytes)."""
+    N, K = W.shape
+    if out is None:
+        out = torch.empty((N, row_bytes(fmt, K)), dtype=torch.uint8, device=W.device)
+    _check(load().bqg_quantize_weights(fmt, _dev(W, "W", torch.float32),
+                                       _dev(out, "out", numel=N * row_bytes(fmt, K)), N, K, _stream(stream)),
+           "bqg_quantize_weights")
+    return out
+
+
+def repack_weights(fmt: int, src: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    size = repacked_size(fmt, N, K)
+    if out is None:
+        out = torch.empty(size, dtype=torch.uint8, device=src.device)
+    _check(load().bqg_repack_weights(fmt, _dev(src, "src", numel=N * row_bytes(fmt, K)),
+                                     _dev(out, "out", numel=size), N, K, _stream(stream)),
+           "bqg_repack_weights")
+    return out
+
+
+# --- per token -----------------------------------------------------------------
+def quantize_q8_1(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16 or fp32 M x K -> q8_1 blocks (uint8, M x K/32*36)."""
+    M, K = x.shape
+    dt = {torch.bfloat16: BF16, torch.float32: F32}.get(x.dtype)
+    if dt is None:
+        raise TypeError("x must be bf16 or fp32")
+    if out is None:
+        out = torch.empty((M, row_bytes(Q8_1, K)), dtype=torch.uint8, device=x.device)
+    _check(load().bqg_quantize_q8_1(_dev(x, "x"), dt, _dev(out, "out", numel=M * row_bytes(Q8_1, K)), M, K,
+                                    _stream(stream)), "bqg_quantize_q8_1")
+    return out
+
+
+def _gemv(fn: str, Wp, X, N: int, K: int, M: int, out, ws, stream, xbytes):
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    wsp, wsb = _ws(ws)
+    _check(getattr(load(), fn)(_dev(Wp, "Wp"), _dev(X, "X", numel=xbytes),
+                               _dev(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)), fn)
+    return out
+
+
+def gemv_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
+    return _gemv("bqg_gemv_bf16", Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
+
+
+def gemv_q8_0(Wp, X, N, K, out=None, ws=None, stream=None):
+    return _gemv("bqg_gemv_q8_0", Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
+
+
+def gemv_q4_0(Wp, X, N, K, out=None, ws=None, stream=None):
+    return _gemv("bqg_gemv_q4_0", Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
+
+
+def gemv_q4_0_q8_1(Wp, Xq, N, K, out=None, ws=None, stream=None):
+    M = Xq.shape[0]
+    return _gemv("bqg_gemv_q4_0_q8_1", Wp, Xq, N, K, M, out, ws, stream, M * row_bytes(Q8_1, K))
+
+
+def gemv_q4_0_q8_1_qkv(Wq, Wk, Wv, Xq, Nq, Nkv, K, out=None, ws=None, stream=None):
+    M = Xq.shape[0]
+    dev = Xq.device
+    if out is None:
+        out = (torch.empty((M, Nq), dtype=torch.float32, device=dev),
+               torch.empty((M, Nkv), dtype=torch.float32, device=dev),
+               torch.empty((M, Nkv), dtype=torch.float32, device=dev))
+    Yq, Yk, Yv = out
+    wsp, wsb = _ws(ws)
+    _check(load().bqg_gemv_q4_0_q8_1_qkv(_dev(Wq, "Wq"), _dev(Wk, "Wk"), _dev(Wv, "Wv"),
+                                         _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
+                                         _dev(Yq, "Yq", torch.float32, M * Nq * 4),
+                                         _dev(Yk, "Yk", torch.float32, M * Nkv * 4),
+                                         _dev(Yv, "Yv", torch.float32, M * Nkv * 4),
+                                         M, Nq, Nkv, K, wsp, wsb, _stream(stream)), "bqg_gemv_q4_0_q8_1_qkv")
+    return out
+
+
+def gemv_q4_0_q8_1_gate_up_swiglu(Wg, Wu, Xq, N, K, out=None, ws=None, stream=None):
+    M = Xq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=Xq.device)
+    wsp, wsb = _ws(ws)
+    _check(load().bqg_gemv_q4_0_q8_1_gate_up_swiglu(_dev(Wg, "Wg"), _dev(Wu, "Wu"),
+                                                    _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
+                                                    _dev(out, "H", torch.float32, M * N * 4), M, N, K, wsp, wsb,
+                                                    _stream(stream)), "bqg_gemv_q4_0_q8_1_gate_up_swiglu")
+    return out
+
+
+def gemm_q4_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
+    M = X.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    wsp, wsb = _ws(ws)
+    _check(load().bqg_gemm_q4_0_bf16(_dev(Wp, "Wp"), _dev(X, "X", torch.bfloat16, M * K * 2),
+                                     _dev(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)),
+           "bqg_gemm_q4_0_bf16")
+    return out
+
+
+def debug_q4_0_q8_1_block_dots(Wp, Xq, N, K, out=None, stream=None):
+    if out is None:
+        out = torch.empty((N, K // QK), dtype=torch.int32, device=Xq.device)
+    _check(load().bqg_debug_q4_0_q8_1_block_dots(_dev(Wp, "Wp"), _dev(Xq, "Xq", numel=row_bytes(Q8_1, K)),
+                                                 _dev(out, "dots", torch.int32, N * (K // QK) * 4), N, K,
+                                                 _stream(stream)), "bqg_debug_q4_0_q8_1_block_dots")
+    return out
+
+
+# --- utilities -----------------------------------------------------------------
+def workspace_size(op: int, M: int, N: int, K: int) -> int:
+    return int(load().bqg_workspace_size(op, M, N, K))
+
+
+def workspace(op: int, M: int, N: int, K: int, device="cuda") -> torch.Tensor | None:
+    n = workspace_size(op, M, N, K)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def last_device_error(stream=None) -> int:
+    out = ctypes.c_int(0)
+    _check(load().bqg_last_device_error(_stream(stream), ctypes.addressof(out)), "bqg_last_device_error")
+    return out.value
+
+
+def set_pdl(enable: bool) -> bool:
+    return bool(load().bqg_set_pdl(1 if enable else 0))

@@ -1,0 +1,407 @@
+// bqg_api.cu -- the C ABI of libbqgemv: argument validation, launch planning
+// and dispatch.  Declarations and contracts: include/bqgemv.h.
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "bqg_gemv.cuh"
+
+namespace bqg {
+cudaError_t gemv_run_bf16(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_run_q8_0(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_run_q4_0(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_run_q4_0_q8_1(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t launch_quantize_q8_1(const void *, int, void *, int, int64_t, cudaStream_t, bool);
+cudaError_t launch_quantize_weights(int, const float *, void *, int64_t, int64_t, cudaStream_t);
+cudaError_t launch_repack(int, const void *, void *, int64_t, int64_t, cudaStream_t);
+cudaError_t launch_block_dots(const void *, const void *, int32_t *, int64_t, int64_t, int64_t, cudaStream_t);
+cudaError_t launch_splitk_reduce(const GemvParams &, int, int, int, cudaStream_t, bool);
+int gemm_q4_0_bf16(const void *, const void *, float *, int, int64_t, int64_t, cudaStream_t, int);
+size_t gemm_workspace(int, int64_t, int64_t);
+int gemm_read_error(cudaStream_t, int *);
+}  // namespace bqg
+
+using namespace bqg;
+
+namespace {
+
+std::atomic<int> g_pdl{0};
+
+struct DevInfo {
+    bool init = false;
+    bool ok = false;
+    int sms = 0;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+std::map<std::tuple<int, int, int, int, int, int, int, size_t>, int> g_occ;
+
+// Current device, checked to be sm_103.
+int current_device(DevInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BQG_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return BQG_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return BQG_ERR_CUDA;
+        d.ok = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.init = true;
+    }
+    *out = d;
+    return d.ok ? BQG_OK : BQG_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool valid_m(int M) { return M == 1 || M == 2 || M == 4 || M == 8; }
+
+int64_t repacked_row_bytes(int fmt, int64_t K)
+{
+    const int64_t nb = K / QK, T = (nb + 31) / 32;
+    if (fmt == BQG_BF16) return 2 * K;
+    if (fmt == BQG_Q4_0) return T * Q4_0_TILE;
+    if (fmt == BQG_Q8_0) return T * Q8_0_TILE;
+    return 0;
+}
+
+// chunk index space of one row (include/bqgemv.h layout, one 16-byte code load per chunk)
+int chunk_space(int wf, int64_t K)
+{
+    const int64_t nb = K / QK, T = (nb + 31) / 32;
+    if (wf == W_BF16) return (int)(K / 8);
+    if (wf == W_Q8_0) return (int)(64 * T);
+    return (int)nb;
+}
+
+using RunFn = cudaError_t (*)(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
+RunFn runner(int wf, int xf)
+{
+    if (xf == X_Q8_1) return gemv_run_q4_0_q8_1;
+    if (wf == W_BF16) return gemv_run_bf16;
+    if (wf == W_Q8_0) return gemv_run_q8_0;
+    return gemv_run_q4_0;
+}
+
+struct GemvPlan {
+    int C, TPR, RG, RB, nc, cps, splits, threads;
+    int64_t rows_per_cta;
+    dim3 grid;
+    size_t smem, ws_bytes;
+};
+
+constexpr int kMaxK = 65536;
+
+// Launch geometry for Nv virtual rows.  `unit` = 2 keeps (gate, up) pairs
+// in one CTA.  Returns a status.
+int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevInfo &dev, int device,
+              GemvPlan *pl)
+{
+    GemvPlan g{};
+    g.nc = chunk_space(wf, K);
+    g.RB = (M == 1) ? 8 : (M == 2) ? 4 : 2;
+    // Split K only when there are too few row batches to give every SM one.
+    g.splits = 1;
+    const int64_t batches = (Nv + g.RB - 1) / g.RB;
+    if (batches < dev.sms) {
+        const int want = (int)((dev.sms + batches - 1) / batches);
+        const int maxs = std::max(1, g.nc / 64);
+        g.splits = std::max(1, std::min(std::min(want, maxs), 16));
+    }
+    g.cps = g.nc;
+    if (g.splits > 1) {
+        g.cps = ((g.nc + g.splits - 1) / g.splits + 31) / 32 * 32;
+        g.splits = (g.nc + g.cps - 1) / g.cps;
+    }
+    g.C = 1;
+    while ((g.cps + g.C - 1) / g.C > 512 && g.C < 4) g.C *= 2;
+    if ((g.cps + g.C - 1) / g.C > 512) return BQG_ERR_UNSUPPORTED_SHAPE;
+    g.TPR = ((g.cps + g.C - 1) / g.C + 31) / 32 * 32;
+    g.RG = std::max(1, std::min(8, 512 / g.TPR));
+    g.threads = g.RG * g.TPR;
+    const int WPG = g.TPR / 32, V = g.RB * M;
+    g.smem = (WPG > 1) ? (size_t)g.RG * 2 * V * WPG * sizeof(float) : 0;
+
+    int bpsm = 0;
+    {
+        auto key = std::make_tuple(device, wf, xf, M, g.C, g.threads, 0, g.smem);
+        std::unique_lock<std::mutex> lk(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) {
+            bpsm = it->second;
+        } else {
+            lk.unlock();
+            GemvParams dummy{};
+            if (runner(wf, xf)(dummy, M, g.C, dim3(1), g.threads, g.smem, 0, false, &bpsm) != cudaSuccess)
+                return BQG_ERR_CUDA;
+            lk.lock();
+            g_occ[key] = bpsm;
+        }
+    }
+    bpsm = std::max(1, bpsm);
+    const int64_t slots = (int64_t)dev.sms * bpsm;
+    int64_t rpc = (Nv * g.splits + slots - 1) / slots;
+    if (unit == 2) rpc = (rpc + 1) / 2 * 2;
+    g.rows_per_cta = std::max<int64_t>(rpc, unit);
+    const int64_t gx = (Nv + g.rows_per_cta - 1) / g.rows_per_cta;
+    if (gx > 0x7fffffff) return BQG_ERR_UNSUPPORTED_SHAPE;
+    g.grid = dim3((unsigned)gx, (unsigned)g.splits);
+    g.ws_bytes = (g.splits > 1) ? (size_t)g.splits * M * Nv * sizeof(float) : 0;
+    *pl = g;
+    return BQG_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? BQG_OK : BQG_ERR_CUDA; }
+
+// Common path of every GEMV entry point.
+int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void *ws, size_t ws_bytes,
+             cudaStream_t stream)
+{
+    DevInfo dev;
+    int dv = 0;
+    int st = current_device(&dev);
+    if (st) return st;
+    cudaGetDevice(&dv);
+    if (p.Nv == 0) return BQG_OK;
+    const int unit = (final_epi == EPI_SWIGLU) ? 2 : 1;
+    GemvPlan g;
+    st = plan_gemv(wf, xf, M, p.Nv, K, unit, dev, dv, &g);
+    if (st) return st;
+    if (g.ws_bytes > 0) {
+        if (!ws || ws_bytes < g.ws_bytes) return BQG_ERR_WORKSPACE;
+        if (!aligned16(ws)) return BQG_ERR_MISALIGNED;
+    }
+    p.K = (int)K;
+    p.nb = (int)(K / QK);
+    p.nc = g.nc;
+    p.TPR = g.TPR;
+    p.RG = g.RG;
+    p.rows_per_cta = g.rows_per_cta;
+    p.chunks_per_split = g.cps;
+    p.ws = (float *)ws;
+    p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;
+    const bool pdl = g_pdl.load() != 0;
+    p.prefetch_rows = pdl ? 8 : 0;
+    cudaError_t e = runner(wf, xf)(p, M, g.C, g.grid, g.threads, g.smem, stream, pdl, nullptr);
+    if (e != cudaSuccess) return BQG_ERR_CUDA;
+    if (g.splits > 1) {
+        e = launch_splitk_reduce(p, M, g.splits, final_epi, stream, pdl);
+        if (e != cudaSuccess) return BQG_ERR_CUDA;
+    }
+    return BQG_OK;
+}
+
+int check_k(int64_t K)
+{
+    if (K <= 0 || K % QK) return BQG_ERR_UNSUPPORTED_SHAPE;
+    if (K > kMaxK) return BQG_ERR_UNSUPPORTED_SHAPE;
+    return BQG_OK;
+}
+
+int gemv_plain(int wf, int xf, int fmt, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
+               void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!Wp || !X || !Y || N < 0 || !valid_m(M)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (wf == W_BF16 && K > 16384) return BQG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(Wp) || !aligned16(Y) || !aligned(X, xf == X_Q8_1 ? 4 : 16)) return BQG_ERR_MISALIGNED;
+    GemvParams p{};
+    p.W[0] = (const uint8_t *)Wp;
+    p.Y[0] = Y;
+    p.rows[0] = N;
+    p.nmat = 1;
+    p.X = (const uint8_t *)X;
+    p.Nv = N;
+    p.row_bytes = repacked_row_bytes(fmt, K);
+    return run_gemv(wf, xf, p, M, K, EPI_STORE, ws, ws_bytes, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bqg_status_string(int s)
+{
+    switch (s) {
+    case BQG_OK: return "ok";
+    case BQG_ERR_INVALID_ARG: return "invalid argument";
+    case BQG_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case BQG_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case BQG_ERR_UNSUPPORTED_DEVICE: return "unsupported device (sm_103 required)";
+    case BQG_ERR_CUDA: return "CUDA error";
+    case BQG_ERR_TIMEOUT: return "bounded device wait timed out";
+    case BQG_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char *bqg_version(void) { return "bqgemv 0.1 sm_103a"; }
+
+int bqg_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
+size_t bqg_repacked_size(int fmt, int64_t N, int64_t K)
+{
+    if (N < 0 || K <= 0 || K % QK) return 0;
+    if (fmt != BQG_BF16 && fmt != BQG_Q8_0 && fmt != BQG_Q4_0) return 0;
+    return (size_t)(N * repacked_row_bytes(fmt, K));
+}
+
+int bqg_quantize_weights(int fmt, const float *W, void *dst, int64_t N, int64_t K, cudaStream_t stream)
+{
+    if (!W || !dst || N < 0 || (fmt != BQG_Q8_0 && fmt != BQG_Q4_0)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (!aligned(W, 4) || !aligned(dst, 2)) return BQG_ERR_MISALIGNED;
+    DevInfo dev;
+    if (int st = current_device(&dev)) return st;
+    if (N == 0) return BQG_OK;
+    return cuda_status(launch_quantize_weights(fmt, W, dst, N, K, stream));
+}
+
+int bqg_repack_weights(int fmt, const void *src, void *dst, int64_t N, int64_t K, cudaStream_t stream)
+{
+    if (!src || !dst || N < 0 || (fmt != BQG_BF16 && fmt != BQG_Q8_0 && fmt != BQG_Q4_0)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (!aligned(src, 2) || !aligned16(dst)) return BQG_ERR_MISALIGNED;
+    DevInfo dev;
+    if (int st = current_device(&dev)) return st;
+    if (N == 0) return BQG_OK;
+    return cuda_status(launch_repack(fmt, src, dst, N, K, stream));
+}
+
+int bqg_quantize_q8_1(const void *x, int x_dtype, void *xq, int M, int64_t K, cudaStream_t stream)
+{
+    if (!x || !xq || M < 1 || M > 65535 || (x_dtype != BQG_BF16 && x_dtype != BQG_F32)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (!aligned(x, x_dtype == BQG_F32 ? 4 : 2) || !aligned(xq, 4)) return BQG_ERR_MISALIGNED;
+    DevInfo dev;
+    if (int st = current_device(&dev)) return st;
+    return cuda_status(launch_quantize_q8_1(x, x_dtype == BQG_F32, xq, M, K, stream, g_pdl.load() != 0));
+}
+
+int bqg_gemv_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
+                  cudaStream_t stream)
+{
+    return gemv_plain(W_BF16, X_BF16, BQG_BF16, Wp, X, Y, M, N, K, ws, ws_bytes, stream);
+}
+
+int bqg_gemv_q8_0(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
+                  cudaStream_t stream)
+{
+    return gemv_plain(W_Q8_0, X_BF16, BQG_Q8_0, Wp, X, Y, M, N, K, ws, ws_bytes, stream);
+}
+
+int bqg_gemv_q4_0(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
+                  cudaStream_t stream)
+{
+    return gemv_plain(W_Q4_0, X_BF16, BQG_Q4_0, Wp, X, Y, M, N, K, ws, ws_bytes, stream);
+}
+
+int bqg_gemv_q4_0_q8_1(const void *Wp, const void *Xq, float *Y, int M, int64_t N, int64_t K, void *ws,
+                       size_t ws_bytes, cudaStream_t stream)
+{
+    return gemv_plain(W_Q4_0, X_Q8_1, BQG_Q4_0, Wp, Xq, Y, M, N, K, ws, ws_bytes, stream);
+}
+
+int bqg_gemv_q4_0_q8_1_qkv(const void *Wq, const void *Wk, const void *Wv, const void *Xq, float *Yq, float *Yk,
+                           float *Yv, int M, int64_t Nq, int64_t Nkv, int64_t K, void *ws, size_t ws_bytes,
+                           cudaStream_t stream)
+{
+    if (!Wq || !Wk || !Wv || !Xq || !Yq || !Yk || !Yv || Nq < 0 || Nkv < 0 || !valid_m(M)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (!aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) || !aligned(Xq, 4) || !aligned16(Yq) || !aligned16(Yk) ||
+        !aligned16(Yv))
+        return BQG_ERR_MISALIGNED;
+    GemvParams p{};
+    p.W[0] = (const uint8_t *)Wq; p.W[1] = (const uint8_t *)Wk; p.W[2] = (const uint8_t *)Wv;
+    p.Y[0] = Yq; p.Y[1] = Yk; p.Y[2] = Yv;
+    p.rows[0] = Nq; p.rows[1] = Nkv; p.rows[2] = Nkv;
+    p.nmat = 3;
+    p.X = (const uint8_t *)Xq;
+    p.Nv = Nq + 2 * Nkv;
+    p.row_bytes = repacked_row_bytes(BQG_Q4_0, K);
+    return run_gemv(W_Q4_0, X_Q8_1, p, M, K, EPI_STORE, ws, ws_bytes, stream);
+}
+
+int bqg_gemv_q4_0_q8_1_gate_up_swiglu(const void *Wg, const void *Wu, const void *Xq, float *H, int M, int64_t N,
+                                      int64_t K, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!Wg || !Wu || !Xq || !H || N < 0 || !valid_m(M)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (!aligned16(Wg) || !aligned16(Wu) || !aligned(Xq, 4) || !aligned16(H)) return BQG_ERR_MISALIGNED;
+    GemvParams p{};
+    p.W[0] = (const uint8_t *)Wg; p.W[1] = (const uint8_t *)Wu;
+    p.Y[0] = H;
+    p.rows[0] = N; p.rows[1] = N;
+    p.nmat = 2;
+    p.X = (const uint8_t *)Xq;
+    p.Nv = 2 * N;
+    p.row_bytes = repacked_row_bytes(BQG_Q4_0, K);
+    return run_gemv(W_Q4_0, X_Q8_1, p, M, K, EPI_SWIGLU, ws, ws_bytes, stream);
+}
+
+int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws,
+                       size_t ws_bytes, cudaStream_t stream)
+{
+    (void)ws; (void)ws_bytes;
+    if (!Wp || !X || !Y || M <= 0 || N < 0) return BQG_ERR_INVALID_ARG;
+    if (M % 128 || N % 128 || K <= 0 || K % 64 || K > kMaxK) return BQG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(Wp) || !aligned16(X) || !aligned16(Y)) return BQG_ERR_MISALIGNED;
+    DevInfo dev;
+    if (int st = current_device(&dev)) return st;
+    if (N == 0) return BQG_OK;
+    return gemm_q4_0_bf16(Wp, X, Y, M, N, K, stream, dev.sms);
+}
+
+int bqg_debug_q4_0_q8_1_block_dots(const void *Wp, const void *Xq, int32_t *dots, int64_t N, int64_t K,
+                                   cudaStream_t stream)
+{
+    if (!Wp || !Xq || !dots || N < 0) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (!aligned16(Wp) || !aligned(Xq, 4) || !aligned(dots, 4)) return BQG_ERR_MISALIGNED;
+    DevInfo dev;
+    if (int st = current_device(&dev)) return st;
+    if (N == 0) return BQG_OK;
+    return cuda_status(launch_block_dots(Wp, Xq, dots, N, K, repacked_row_bytes(BQG_Q4_0, K), stream));
+}
+
+size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K)
+{
+    if (N <= 0 || K <= 0 || K % QK || K > kMaxK) return 0;
+    if (op == BQG_OP_GEMM_Q4_0_BF16) return gemm_workspace(M, N, K);
+    if (!valid_m(M)) return 0;
+    DevInfo dev;
+    int dv = 0;
+    if (current_device(&dev) != BQG_OK) return 0;
+    cudaGetDevice(&dv);
+    int wf = W_Q4_0, xf = X_Q8_1, unit = 1;
+    int64_t Nv = N;
+    switch (op) {
+    case BQG_OP_GEMV_BF16: wf = W_BF16; xf = X_BF16; break;
+    case BQG_OP_GEMV_Q8_0: wf = W_Q8_0; xf = X_BF16; break;
+    case BQG_OP_GEMV_Q4_0: wf = W_Q4_0; xf = X_BF16; break;
+    case BQG_OP_GEMV_Q4_0_Q8_1: break;
+    case BQG_OP_QKV_Q4_0_Q8_1: break;
+    case BQG_OP_GATE_UP_Q4_0_Q8_1: Nv = 2 * N; unit = 2; break;
+    default: return 0;
+    }
+    GemvPlan g;
+    if (plan_gemv(wf, xf, M, Nv, K, unit, dev, dv, &g) != BQG_OK) return 0;
+    return g.ws_bytes;
+}
+
+int bqg_last_device_error(cudaStream_t stream, int *out)
+{
+    if (!out) return BQG_ERR_INVALID_ARG;
+    return gemm_read_error(stream, out);
+}
+
+}  // extern "C"

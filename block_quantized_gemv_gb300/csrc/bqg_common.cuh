@@ -1,0 +1,120 @@
+// bqg_common.cuh -- device helpers shared by the sm_103a kernels of libbqgemv.
+//
+// Block formats (32 elements per block) and the repacked weight layout are
+// described in include/bqgemv.h.  Nothing here is shared with the CPU oracle.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "../../include/bqgemv.h"
+
+namespace bqg {
+
+constexpr int QK = 32;              // elements per block
+constexpr int Q8_0_BYTES = 34;
+constexpr int Q4_0_BYTES = 18;
+constexpr int Q8_1_BYTES = 36;
+constexpr int Q4_0_TILE = 576;      // 32 blocks: 512 B codes + 64 B scales
+constexpr int Q8_0_TILE = 1088;     // 32 blocks: 1024 B codes + 64 B scales
+
+// ---------------------------------------------------------------------------
+// loads
+// ---------------------------------------------------------------------------
+// Weights are read exactly once per call: read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream_v4(const void *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream_u16(const void *p)
+{
+    unsigned short v;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void *p)
+{
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Warm L2 with a contiguous byte range (no data is consumed, so it is safe
+// to issue before the previous grid on the stream has finished).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: no-ops when the kernel was launched
+// without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// scalar conversions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// Byte j of `w` (an unsigned code u) as the exact float u + 2^23, built by
+// placing u in the mantissa of 2^23 (one byte permute, no int->float unit).
+template <int J>
+__device__ __forceinline__ float byte_plus_2p23(uint32_t w)
+{
+    return __uint_as_float(__byte_perm(w, 0x4b000000u, J | (4 << 4) | (4 << 8) | (7 << 12)));
+}
+
+// ---------------------------------------------------------------------------
+// warp reductions
+// ---------------------------------------------------------------------------
+// Reduce V values per lane over the 32 lanes of a warp by recursive halving:
+// after log2(V) exchange steps each lane keeps one partial of index
+// (lane >> (5 - log2 V)) & (V - 1), then a butterfly over the remaining lane
+// bits completes it.  The full sum of value i ends in lane i << (5 - log2 V).
+// V must be a power of two <= 32.  Cost: V - 1 + (5 - log2 V) shuffles.
+template <int V>
+struct WarpReduce {
+    static constexpr int L = (V >= 32) ? 5 : (V >= 16) ? 4 : (V >= 8) ? 3 : (V >= 4) ? 2 : (V >= 2) ? 1 : 0;
+    static_assert((1 << L) == V, "V must be a power of two <= 32");
+
+    __device__ __forceinline__ static float run(float (&v)[V], int lane)
+    {
+#pragma unroll
+        for (int step = 0; step < L; step++) {
+            const int off = 16 >> step;
+            const int half = V >> (step + 1);
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int j = 0; j < half; j++) {
+                float send = upper ? v[j] : v[j + half];
+                float keep = upper ? v[j + half] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+        }
+        float s = v[0];
+#pragma unroll
+        for (int off = 16 >> L; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        return s;
+    }
+    __device__ __forceinline__ static int index_of_lane(int lane) { return (lane >> (5 - L)) & (V - 1); }
+    __device__ __forceinline__ static int lane_of_index(int i) { return i << (5 - L); }
+    __device__ __forceinline__ static bool is_holder(int lane) { return (lane & ((32 >> L) - 1)) == 0; }
+};
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace bqg

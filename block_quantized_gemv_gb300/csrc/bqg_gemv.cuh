@@ -1,0 +1,460 @@
+// bqg_gemv.cuh -- the skinny-GEMV kernel template (M = 1, 2, 4, 8).
+//
+// Y[m, n] = sum_k W[n, k] X[m, k] for the memory-bound decode shape of
+// "The Shape That Actually Matters" (M = 1, K = 4096, N = 12288 and the
+// rest of the decode projections).  Design for sm_103a:
+//
+//  * Weights are the only large stream.  They are read once, with 128-bit
+//    non-allocating loads from the repacked layout (include/bqgemv.h), so
+//    every warp-wide load instruction covers 512 contiguous bytes and the
+//    fp16 scales come from the same tile ("Rounds 1-3" of that page: the
+//    layout and the load width, not the byte count, decided the bandwidth).
+//  * Each thread owns a fixed slice of K ("chunks") for every row it
+//    visits, so its slice of the activation rows is loaded into registers
+//    once per CTA and never re-read ("MI50 megakernel", microbenchmark
+//    ladder: re-loading the activation was three of five memory
+//    instructions per iteration).
+//  * A row group of TPR threads covers one row's K range; RB rows are in
+//    flight per thread, so one warp-wide reduction (recursive halving, one
+//    shuffle per value) serves RB*M outputs; groups of more than one warp
+//    finish through shared memory and a named barrier.
+//  * Each CTA owns a contiguous range of rows; the grid is sized from the
+//    SM count and the measured occupancy.  Split-K (grid.y > 1) writes
+//    partial sums to a workspace reduced by gemv_splitk_reduce.
+//  * q4_0 x q8_1 multiplies codes with dp4a: per block the integer dot
+//    sum (qw - 8) qx is exact ("rx-6700xt-llama2-decode": integer-dot
+//    Q4_0 x Q8_1 matvec), scaled by d_w d_x in fp32.
+#pragma once
+
+#include "bqg_common.cuh"
+
+namespace bqg {
+
+enum WFmt { W_BF16 = 0, W_Q8_0 = 1, W_Q4_0 = 2 };
+enum XFmt { X_BF16 = 0, X_Q8_1 = 1 };
+enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_PARTIAL = 2 };
+
+// elements covered by one chunk (one 16-byte code load)
+template <int WF> struct ChunkTraits;
+template <> struct ChunkTraits<W_BF16> { static constexpr int E = 8; };
+template <> struct ChunkTraits<W_Q8_0> { static constexpr int E = 16; };
+template <> struct ChunkTraits<W_Q4_0> { static constexpr int E = 32; };
+
+struct GemvParams {
+    // up to three weight matrices in one "virtual" row space
+    const uint8_t *W[3];
+    float *Y[3];
+    int64_t rows[3];        // rows of each matrix
+    int nmat;               // 1, 2 (gate/up, rows interleaved g0 u0 g1 u1 ...) or 3 (q, k, v)
+    int epi;                // Epi
+    const uint8_t *X;       // bf16 [M][K] or q8_1 [M][K/32]
+    float *ws;              // split-K partials [splits][M][Nv]
+    int64_t Nv;             // virtual rows
+    int64_t row_bytes;      // bytes of one repacked row
+    int K;
+    int nb;                 // K / 32
+    int nc;                 // chunks per row (chunk index space, may contain holes)
+    int TPR;                // threads per row group (multiple of 32)
+    int RG;                 // row groups per CTA
+    int64_t rows_per_cta;   // virtual rows per CTA (multiple of 2 for gate/up)
+    int chunks_per_split;   // chunk range of one split (grid.y)
+    int prefetch_rows;      // rows of this CTA to warm in L2 before griddepcontrol.wait
+};
+
+// Virtual row -> (matrix, row in matrix)
+__device__ __forceinline__ void map_row(const GemvParams &p, int64_t v, int &mat, int64_t &r)
+{
+    if (p.nmat == 2) { mat = (int)(v & 1); r = v >> 1; return; }
+    mat = 0; r = v;
+    if (p.nmat == 3) {
+        if (r >= p.rows[0]) { r -= p.rows[0]; mat = 1;
+            if (r >= p.rows[1]) { r -= p.rows[1]; mat = 2; } }
+    }
+}
+
+// Is chunk c of a row a real chunk (not a hole in a partly used last tile)?
+template <int WF>
+__device__ __forceinline__ bool chunk_valid(int c, int nb, int nc)
+{
+    if (c >= nc) return false;
+    if (WF == W_Q8_0) return (c >> 6) * 32 + (c & 31) < nb;
+    if (WF == W_Q4_0) return c < nb;
+    return true;
+}
+
+// Byte offset of chunk c's codes within a repacked row, and of its scale.
+template <int WF>
+__device__ __forceinline__ int64_t chunk_code_off(int c)
+{
+    if (WF == W_BF16) return 16ll * c;
+    if (WF == W_Q8_0) return (int64_t)(c >> 6) * Q8_0_TILE + ((c >> 5) & 1) * 512 + 16 * (c & 31);
+    return (int64_t)(c >> 5) * Q4_0_TILE + 16 * (c & 31);
+}
+template <int WF>
+__device__ __forceinline__ int64_t chunk_scale_off(int c)
+{
+    if (WF == W_Q8_0) return (int64_t)(c >> 6) * Q8_0_TILE + 1024 + 2 * (c & 31);
+    return (int64_t)(c >> 5) * Q4_0_TILE + 512 + 2 * (c & 31);
+}
+// First element of chunk c along K.
+template <int WF>
+__device__ __forceinline__ int chunk_elem0(int c)
+{
+    if (WF == W_BF16) return 8 * c;
+    if (WF == W_Q8_0) return 32 * ((c >> 6) * 32 + (c & 31)) + 16 * ((c >> 5) & 1);
+    return 32 * c;
+}
+
+// ---------------------------------------------------------------------------
+// per-thread activation slice
+// ---------------------------------------------------------------------------
+template <int WF, int XF> struct XSlice;
+// bf16 activations: E bf16 values per chunk, kept packed (E/2 words)
+template <int WF> struct XSlice<WF, X_BF16> {
+    static constexpr int WORDS = ChunkTraits<WF>::E / 2;
+    uint32_t w[WORDS];
+};
+// q8_1 activations (q4_0 weights only): 32 codes, d, and the exact sum of codes
+template <> struct XSlice<W_Q4_0, X_Q8_1> {
+    int32_t q[8];
+    float d;
+    int32_t sum;
+};
+
+template <int WF, int XF>
+__device__ __forceinline__ void load_x(XSlice<WF, XF> &xs, const GemvParams &p, int m, int c, bool valid)
+{
+    if constexpr (XF == X_BF16) {
+        constexpr int WORDS = XSlice<WF, XF>::WORDS;
+        if (!valid) {
+#pragma unroll
+            for (int i = 0; i < WORDS; i++) xs.w[i] = 0;
+            return;
+        }
+        const uint8_t *src = p.X + ((int64_t)m * p.K + chunk_elem0<WF>(c)) * 2;
+#pragma unroll
+        for (int i = 0; i < WORDS / 4; i++) {
+            uint4 v = ldg_v4(src + 16 * i);
+            xs.w[4 * i + 0] = v.x; xs.w[4 * i + 1] = v.y; xs.w[4 * i + 2] = v.z; xs.w[4 * i + 3] = v.w;
+        }
+    } else {
+        if (!valid) {
+#pragma unroll
+            for (int i = 0; i < 8; i++) xs.q[i] = 0;
+            xs.d = 0.f; xs.sum = 0;
+            return;
+        }
+        // q8_1 block: fp16 d | fp16 s | int8 q[32]; rows of 36-byte blocks are
+        // only 4-byte aligned, so read words.
+        const uint32_t *blk = reinterpret_cast<const uint32_t *>(p.X + ((int64_t)m * p.nb + c) * Q8_1_BYTES);
+        uint32_t ds = __ldg(blk);
+        xs.d = half_bits_to_float(ds & 0xffffu);
+        int s = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            xs.q[i] = (int32_t)__ldg(blk + 1 + i);
+            s = __dp4a(xs.q[i], 0x01010101, s);    // exact sum of the 32 codes
+        }
+        xs.sum = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// per-thread weight chunk
+// ---------------------------------------------------------------------------
+template <int WF> struct WChunk { uint4 c; uint32_t s; };
+
+template <int WF>
+__device__ __forceinline__ void load_w(WChunk<WF> &w, const uint8_t *row, int c, bool valid)
+{
+    if (!valid) { w.c = make_uint4(0, 0, 0, 0); w.s = 0; return; }
+    w.c = ldg_stream_v4(row + chunk_code_off<WF>(c));
+    if constexpr (WF != W_BF16) w.s = ldg_stream_u16(row + chunk_scale_off<WF>(c));
+    else w.s = 0;
+}
+
+// Exact per-block integer dot of a q4_0 code chunk with a q8_1 block:
+// sum_i (qw_i - 8) qx_i.  Word i of the codes holds elements 4i..4i+3 in its
+// low nibbles and 16+4i..16+4i+3 in its high nibbles; x.q[i] holds codes
+// 4i..4i+3.  |result| <= 32 * 8 * 127.
+__device__ __forceinline__ int q4_0_q8_1_sumi(const uint4 &c, const XSlice<W_Q4_0, X_Q8_1> &x)
+{
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++) s = __dp4a((int)(cw[i] & 0x0f0f0f0fu), x.q[i], s);
+#pragma unroll
+    for (int i = 0; i < 4; i++) s = __dp4a((int)((cw[i] >> 4) & 0x0f0f0f0fu), x.q[4 + i], s);
+    return s - 8 * x.sum;
+}
+
+// dot(chunk, activation slice) in fp32
+template <int WF, int XF>
+__device__ __forceinline__ float chunk_dot(const WChunk<WF> &w, const XSlice<WF, XF> &x)
+{
+    const uint32_t cw[4] = {w.c.x, w.c.y, w.c.z, w.c.w};
+    if constexpr (WF == W_BF16) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            a0 = fmaf(bf16_lo(cw[i]), bf16_lo(x.w[i]), a0);
+            a1 = fmaf(bf16_hi(cw[i]), bf16_hi(x.w[i]), a1);
+        }
+        return a0 + a1;
+    } else if constexpr (WF == W_Q8_0) {
+        // codes are int8 q; byte ^ 0x80 = q + 128 as an unsigned byte
+        constexpr float OFF = 8388608.0f + 128.0f;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t u = cw[i] ^ 0x80808080u;
+            a0 = fmaf(byte_plus_2p23<0>(u) - OFF, bf16_lo(x.w[2 * i]), a0);
+            a1 = fmaf(byte_plus_2p23<1>(u) - OFF, bf16_hi(x.w[2 * i]), a1);
+            a0 = fmaf(byte_plus_2p23<2>(u) - OFF, bf16_lo(x.w[2 * i + 1]), a0);
+            a1 = fmaf(byte_plus_2p23<3>(u) - OFF, bf16_hi(x.w[2 * i + 1]), a1);
+        }
+        return (a0 + a1) * half_bits_to_float(w.s);
+    } else if constexpr (XF == X_BF16) {
+        // q4_0 x bf16: word i holds elements 4i..4i+3 (low nibbles) and
+        // 16+4i..16+4i+3 (high nibbles); x.w[k] holds elements 2k, 2k+1.
+        constexpr float OFF = 8388608.0f + 8.0f;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t lo = cw[i] & 0x0f0f0f0fu;
+            const uint32_t hi = (cw[i] >> 4) & 0x0f0f0f0fu;
+            a0 = fmaf(byte_plus_2p23<0>(lo) - OFF, bf16_lo(x.w[2 * i]), a0);
+            a1 = fmaf(byte_plus_2p23<1>(lo) - OFF, bf16_hi(x.w[2 * i]), a1);
+            a0 = fmaf(byte_plus_2p23<2>(lo) - OFF, bf16_lo(x.w[2 * i + 1]), a0);
+            a1 = fmaf(byte_plus_2p23<3>(lo) - OFF, bf16_hi(x.w[2 * i + 1]), a1);
+            a0 = fmaf(byte_plus_2p23<0>(hi) - OFF, bf16_lo(x.w[8 + 2 * i]), a0);
+            a1 = fmaf(byte_plus_2p23<1>(hi) - OFF, bf16_hi(x.w[8 + 2 * i]), a1);
+            a0 = fmaf(byte_plus_2p23<2>(hi) - OFF, bf16_lo(x.w[8 + 2 * i + 1]), a0);
+            a1 = fmaf(byte_plus_2p23<3>(hi) - OFF, bf16_hi(x.w[8 + 2 * i + 1]), a1);
+        }
+        return (a0 + a1) * half_bits_to_float(w.s);
+    } else {
+        // q4_0 x q8_1: exact integer dot, then one fp32 scale
+        return (half_bits_to_float(w.s) * x.d) * (float)q4_0_q8_1_sumi(w.c, x);
+    }
+}
+
+__device__ __forceinline__ void named_barrier(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// rows in flight per thread for each M (RB * M values are reduced per batch)
+template <int M> struct RowsPerBatch { static constexpr int value = (M == 1) ? 8 : (M == 2) ? 4 : 2; };
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int WF, int XF, int M, int C>
+__global__ void __launch_bounds__(512) gemv_kernel(const GemvParams p)
+{
+    constexpr int RB = RowsPerBatch<M>::value;
+    constexpr int V = RB * M;
+    using WR = WarpReduce<V>;
+    extern __shared__ float sred[];        // [RG][2][V][WPG] when a group has > 1 warp
+
+    const int tid = threadIdx.x;
+    const int g = tid / p.TPR;             // row group
+    const int tau = tid - g * p.TPR;       // thread in group
+    const int lane = tid & 31;
+    const int wig = tau >> 5;              // warp in group
+    const int WPG = p.TPR >> 5;
+
+    const int64_t v0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int64_t v1 = min(p.Nv, v0 + p.rows_per_cta);
+    const int split = blockIdx.y;
+    const int cbeg = split * p.chunks_per_split;
+    const int cend = min(p.nc, cbeg + p.chunks_per_split);
+
+    int cid[C];
+    bool cval[C];
+#pragma unroll
+    for (int i = 0; i < C; i++) {
+        cid[i] = cbeg + tau + i * p.TPR;
+        cval[i] = cid[i] < cend && chunk_valid<WF>(cid[i], p.nb, p.nc);
+    }
+
+    // Before waiting for the previous grid: warm L2 with the first rows of
+    // this CTA (weights do not depend on that grid; nothing is consumed).
+    if (p.prefetch_rows > 0) {
+        const int64_t npf = min((int64_t)p.prefetch_rows, v1 - v0);
+        for (int64_t j = tid; j < npf; j += blockDim.x) {
+            int mat; int64_t rr;
+            map_row(p, v0 + j, mat, rr);
+            prefetch_l2_bulk(p.W[mat] + rr * p.row_bytes, (uint32_t)p.row_bytes);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+
+    XSlice<WF, XF> xs[C][M];
+#pragma unroll
+    for (int i = 0; i < C; i++)
+#pragma unroll
+        for (int m = 0; m < M; m++) load_x<WF, XF>(xs[i][m], p, m, cid[i], cval[i]);
+
+    // Group g visits units g, g + RG, g + 2 RG, ... of this CTA's rows; a unit
+    // is one row, or a (gate, up) row pair for the SwiGLU epilogue.  RB rows
+    // (RB / U units) are in flight per thread.
+    const int U = (p.epi == EPI_SWIGLU || p.nmat == 2) ? 2 : 1;
+    auto row_of = [&](int64_t i0, int r) -> int64_t {
+        return v0 + (g + (int64_t)p.RG * (i0 + r / U)) * U + (r % U);
+    };
+    WChunk<WF> wc[RB][C];
+    int64_t i0 = 0;
+    const int64_t di = RB / U;
+    if (row_of(0, 0) < v1) {
+#pragma unroll
+        for (int r = 0; r < RB; r++) {
+            const int64_t v = row_of(0, r);
+            const bool rv = v < v1;
+            const uint8_t *row = nullptr;
+            if (rv) { int mat; int64_t rr; map_row(p, v, mat, rr); row = p.W[mat] + rr * p.row_bytes; }
+#pragma unroll
+            for (int i = 0; i < C; i++) load_w<WF>(wc[r][i], row, cid[i], rv && cval[i]);
+        }
+    }
+    int buf = 0;
+    for (; row_of(i0, 0) < v1; i0 += di) {
+        float acc[V];
+#pragma unroll
+        for (int r = 0; r < RB; r++)
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                float a = 0.f;
+#pragma unroll
+                for (int i = 0; i < C; i++) a += chunk_dot<WF, XF>(wc[r][i], xs[i][m]);
+                acc[r * M + m] = a;
+            }
+        // issue the next batch before reducing this one
+        if (row_of(i0 + di, 0) < v1) {
+#pragma unroll
+            for (int r = 0; r < RB; r++) {
+                const int64_t v = row_of(i0 + di, r);
+                const bool rv = v < v1;
+                const uint8_t *row = nullptr;
+                if (rv) { int mat; int64_t rr; map_row(p, v, mat, rr); row = p.W[mat] + rr * p.row_bytes; }
+#pragma unroll
+                for (int i = 0; i < C; i++) load_w<WF>(wc[r][i], row, cid[i], rv && cval[i]);
+            }
+        }
+
+        float tot = WR::run(acc, lane);
+        int idx = WR::index_of_lane(lane);
+        bool holder = WR::is_holder(lane);
+        bool finals_here = true;            // does this warp hold the finished sums?
+        if (WPG > 1) {
+            float *slot = sred + (size_t)(g * 2 + buf) * V * WPG;
+            if (holder) slot[idx * WPG + wig] = tot;
+            named_barrier(1 + g, p.TPR);
+            finals_here = (wig == 0);
+            if (finals_here) {
+                float s = 0.f;
+                if (lane < V)
+                    for (int w = 0; w < WPG; w++) s += slot[lane * WPG + w];
+                tot = s;
+                idx = lane;
+                holder = lane < V;
+            }
+            buf ^= 1;
+        }
+        if (finals_here) {
+            const int r = idx / M, m = idx - (idx / M) * M;
+            const int64_t v = row_of(i0, r);
+            if (p.epi == EPI_SWIGLU) {
+                // (gate, up) rows alternate; batches start on even rows
+                const int pidx = min(idx + M, V - 1);
+                const int plane = (WPG > 1) ? pidx : WR::lane_of_index(pidx);
+                const float u = __shfl_sync(0xffffffffu, tot, plane);
+                if (holder && (r & 1) == 0 && v < v1)
+                    p.Y[0][(int64_t)m * p.rows[0] + (v >> 1)] = silu(tot) * u;
+            } else if (p.epi == EPI_PARTIAL) {
+                if (holder && v < v1) p.ws[((int64_t)split * M + m) * p.Nv + v] = tot;
+            } else {
+                if (holder && v < v1) {
+                    int mat; int64_t rr;
+                    map_row(p, v, mat, rr);
+                    p.Y[mat][(int64_t)m * p.rows[mat] + rr] = tot;
+                }
+            }
+        }
+    }
+}
+
+// Split-K finish: Y = sum over splits (in split order) of the partials,
+// then the same epilogue as the single-pass kernel.
+static __global__ void __launch_bounds__(256) gemv_splitk_reduce(const GemvParams p, int M, int splits, int final_epi)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (final_epi == EPI_SWIGLU) {
+        const int64_t np = p.Nv >> 1;
+        if (i >= (int64_t)M * np) return;
+        const int64_t m = i / np, pr = i - (i / np) * np;
+        float gs = 0.f, us = 0.f;
+        for (int s = 0; s < splits; s++) {
+            gs += p.ws[((int64_t)s * M + m) * p.Nv + 2 * pr];
+            us += p.ws[((int64_t)s * M + m) * p.Nv + 2 * pr + 1];
+        }
+        p.Y[0][m * p.rows[0] + pr] = silu(gs) * us;
+    } else {
+        if (i >= (int64_t)M * p.Nv) return;
+        const int64_t m = i / p.Nv, v = i - (i / p.Nv) * p.Nv;
+        float s = 0.f;
+        for (int k = 0; k < splits; k++) s += p.ws[((int64_t)k * M + m) * p.Nv + v];
+        int mat; int64_t rr;
+        map_row(p, v, mat, rr);
+        p.Y[mat][m * p.rows[mat] + rr] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host-side launch helpers (one instantiation set per translation unit)
+// ---------------------------------------------------------------------------
+template <int WF, int XF, int M, int C>
+__host__ cudaError_t gemv_launch_one(const GemvParams &p, dim3 grid, int threads, size_t smem,
+                                     cudaStream_t stream, bool pdl, int *occupancy)
+{
+    auto kern = gemv_kernel<WF, XF, M, C>;
+    if (occupancy) {
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, threads, smem);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int WF, int XF>
+__host__ cudaError_t gemv_dispatch(const GemvParams &p, int M, int C, dim3 grid, int threads, size_t smem,
+                                   cudaStream_t stream, bool pdl, int *occupancy)
+{
+#define BQG_CASE(MM, CC)                                                                 \
+    if (M == MM && C == CC)                                                              \
+        return gemv_launch_one<WF, XF, MM, CC>(p, grid, threads, smem, stream, pdl, occupancy);
+    BQG_CASE(1, 1) BQG_CASE(1, 2) BQG_CASE(1, 4)
+    BQG_CASE(2, 1) BQG_CASE(2, 2) BQG_CASE(2, 4)
+    BQG_CASE(4, 1) BQG_CASE(4, 2) BQG_CASE(4, 4)
+    BQG_CASE(8, 1) BQG_CASE(8, 2) BQG_CASE(8, 4)
+#undef BQG_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace bqg

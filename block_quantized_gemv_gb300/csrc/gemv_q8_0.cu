@@ -1,0 +1,10 @@
+// gemv_q8_0.cu -- instantiations of the skinny-GEMV kernel for W_Q8_0 weights x X_BF16 activations.
+#include "bqg_gemv.cuh"
+
+namespace bqg {
+cudaError_t gemv_run_q8_0(const GemvParams &p, int M, int C, dim3 grid, int threads, size_t smem,
+                        cudaStream_t stream, bool pdl, int *occupancy)
+{
+    return gemv_dispatch<W_Q8_0, X_BF16>(p, M, C, grid, threads, smem, stream, pdl, occupancy);
+}
+}  // namespace bqg

@@ -1,0 +1,195 @@
+/*
+ * bqgemv.h -- block-quantized skinny GEMV / prefill GEMM for GB300 (sm_103a).
+ *
+ * What it computes (all entry points):
+ *     Y[m, n] = sum_k  W[n, k] * X[m, k]          m < M, n < N, k < K
+ * with W stored as N rows of K weights and X as M rows of K activations:
+ * the memory-bound decode shape (M = 1..8) of "The Shape That Actually
+ * Matters" (amarbaro.com), and the M = 512 prefill GEMM over dequantized
+ * weight tiles of "llama-3x-prompt-speed" ("the tile").  Outputs are fp32.
+ *
+ * Block formats (32 elements per block, little-endian fp16 scales):
+ *   BQG_Q8_0  34 B = fp16 d | int8 q[32]                  w = q * d
+ *   BQG_Q4_0  18 B = fp16 d | 16 bytes of 4-bit codes      w = (q - 8) * d
+ *             (the 18-byte block of "MI50 megakernel", hypothesis ledger;
+ *              byte j holds element j in its low nibble, j+16 in its high)
+ *   BQG_Q8_1  36 B = fp16 d | fp16 s | int8 q[32]          x = q * d,
+ *             s = fp16(d * sum q)   (the activation side of the "Q4_0 x Q8_1"
+ *             matvec of "rx-6700xt-llama2-decode", Approach & Methodology)
+ *   BQG_BF16  2 B per element, no blocks.
+ * A "canonical" weight matrix is N rows, each K/32 consecutive blocks.
+ *
+ * Repacked weights (the layout every GEMV/GEMM entry point reads), produced
+ * once at load time by bqg_repack_weights.  nb = K/32 blocks per row,
+ * T = ceil(nb/32) tiles per row, a tile = 32 consecutive blocks of one row:
+ *   bf16 : row-major N x K, identical to canonical.
+ *   q4_0 : tile of 576 B: block 32t+s has its 16 code bytes at 16*s and its
+ *          fp16 scale at 512 + 2*s.
+ *   q8_0 : tile of 1088 B: block 32t+s has codes 0..15 at 16*s, codes 16..31
+ *          at 512 + 16*s, and its fp16 scale at 1024 + 2*s.
+ * Rows follow each other with a stride of T tiles; unused slots of a row's
+ * last tile are zero.  Every 32 lanes of a warp then read 512 contiguous
+ * bytes per 128-bit load, and scales sit beside their codes.
+ *
+ * Rounding rules of the encoders (the pages name the formats only):
+ *   the scale is computed in fp32 and rounded once to fp16 (nearest-even);
+ *   codes divide by the STORED fp16 scale in IEEE fp32 and round half away
+ *   from zero; q8: d = amax/127, q clamped to [-127, 127], d = 0 gives q = 0;
+ *   q4_0: m = first element of largest |x|, d = m / -8,
+ *         q = clamp(round(x/d) + 8, 0, 15), d = 0 gives q = 8.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers on the current CUDA device unless stated.
+ *     The caller owns every buffer; the library never allocates, frees or
+ *     keeps a pointer after the call returns.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *     returns a bqg_status.  Arguments are validated on the host before any
+ *     launch; an invalid call launches nothing.
+ *   - Device pointers must be 16-byte aligned (BQG_ERR_MISALIGNED otherwise).
+ *   - K must be a positive multiple of 32 (BQG_ERR_UNSUPPORTED_SHAPE).
+ *   - Only sm_103 devices are accepted (BQG_ERR_UNSUPPORTED_DEVICE).
+ *   - There is no CPU fallback and no silent change of route.
+ */
+#ifndef BQGEMV_H
+#define BQGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* formats */
+enum { BQG_BF16 = 0, BQG_Q8_0 = 1, BQG_Q4_0 = 2, BQG_Q8_1 = 3, BQG_F32 = 4 };
+
+/* status codes */
+enum {
+    BQG_OK = 0,
+    BQG_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, M not allowed, N < 0 */
+    BQG_ERR_UNSUPPORTED_SHAPE = 2,  /* K % 32 != 0, K or M beyond the kernel limits */
+    BQG_ERR_MISALIGNED = 3,         /* a device pointer is not 16-byte aligned      */
+    BQG_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103                 */
+    BQG_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed         */
+    BQG_ERR_TIMEOUT = 6,            /* a bounded device-side wait gave up           */
+    BQG_ERR_WORKSPACE = 7           /* the call needs a workspace that is missing   */
+};
+
+/* operation ids for bqg_workspace_size */
+enum {
+    BQG_OP_GEMV_BF16 = 0,
+    BQG_OP_GEMV_Q8_0 = 1,
+    BQG_OP_GEMV_Q4_0 = 2,
+    BQG_OP_GEMV_Q4_0_Q8_1 = 3,
+    BQG_OP_QKV_Q4_0_Q8_1 = 4,       /* N = Nq + 2*Nkv */
+    BQG_OP_GATE_UP_Q4_0_Q8_1 = 5,   /* N = rows of each of gate and up */
+    BQG_OP_GEMM_Q4_0_BF16 = 6
+};
+
+/* ---- load time ------------------------------------------------------- */
+
+/* Bytes of the repacked layout of an N x K matrix of `fmt` (BQG_BF16,
+ * BQG_Q8_0 or BQG_Q4_0); 0 for an invalid format or K % 32 != 0. */
+size_t bqg_repacked_size(int fmt, int64_t N, int64_t K);
+
+/* Encode fp32 weights (N x K, row-major, device) into canonical q8_0 or
+ * q4_0 blocks (N x K/32 blocks, device) with the rounding rules above.
+ * fmt: BQG_Q8_0 or BQG_Q4_0.  `dst` needs N*(K/32)*(34 or 18) bytes and
+ * may be 2-byte aligned (block rows are not 16-byte multiples). */
+int bqg_quantize_weights(int fmt, const float *W, void *dst, int64_t N, int64_t K,
+                         cudaStream_t stream);
+
+/* Canonical -> repacked layout (above).  `src` canonical (2-byte aligned is
+ * enough), `dst` bqg_repacked_size(fmt, N, K) bytes, 16-byte aligned; the
+ * two must not overlap.  Pure byte permutation (bit-exact). */
+int bqg_repack_weights(int fmt, const void *src, void *dst, int64_t N, int64_t K,
+                       cudaStream_t stream);
+
+/* ---- per token -------------------------------------------------------- */
+
+/* Quantize activations to q8_1 blocks ("Q8_1" of rx-6700xt-llama2-decode).
+ * x: M x K, x_dtype BQG_BF16 or BQG_F32, row-major.  xq: M x K/32 blocks of
+ * 36 B, row-major.  1 <= M <= 65535.  Bit-exact with the rules above. */
+int bqg_quantize_q8_1(const void *x, int x_dtype, void *xq, int M, int64_t K,
+                      cudaStream_t stream);
+
+/* Skinny GEMV, M in {1, 2, 4, 8}.  Wp: repacked weights of the named format.
+ * X: M x K bf16 (row-major).  Y: M x N fp32 (row-major).
+ * ws/ws_bytes: workspace for split-K; bqg_workspace_size(op, M, N, K) bytes
+ * are required when that size is non-zero (BQG_ERR_WORKSPACE otherwise); it
+ * needs no initialisation and must not be shared by calls that overlap.
+ * fp32 accumulation; bqg_gemv_q8_0/q4_0 dequantize (q*d, (q-8)*d) exactly. */
+int bqg_gemv_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
+                  void *ws, size_t ws_bytes, cudaStream_t stream);
+int bqg_gemv_q8_0(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
+                  void *ws, size_t ws_bytes, cudaStream_t stream);
+int bqg_gemv_q4_0(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
+                  void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* q4_0 weights x q8_1 activations (M in {1, 2, 4, 8}).  Per block the
+ * integer dot sumi = sum_i (qw_i - 8) * qx_i is exact (int32, dp4a), and
+ * Y += (d_w * d_x) * sumi in fp32.  Xq: M x K/32 q8_1 blocks. */
+int bqg_gemv_q4_0_q8_1(const void *Wp, const void *Xq, float *Y, int M, int64_t N, int64_t K,
+                       void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Q, K and V projections of one shared activation in a single launch
+ * (the grouped QKV launch of "rx-6700xt-llama2-decode", Approach &
+ * Methodology).  Wq: Nq x K, Wk/Wv: Nkv x K repacked q4_0;
+ * Yq: M x Nq, Yk/Yv: M x Nkv fp32.  Same arithmetic as bqg_gemv_q4_0_q8_1. */
+int bqg_gemv_q4_0_q8_1_qkv(const void *Wq, const void *Wk, const void *Wv, const void *Xq,
+                           float *Yq, float *Yk, float *Yv, int M, int64_t Nq, int64_t Nkv,
+                           int64_t K, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Feed-forward gate and up projections in one launch with the SwiGLU
+ * epilogue applied before the store (the grouped feed-forward launch of
+ * "rx-6700xt-llama2-decode", Approach & Methodology):
+ * H[m, n] = silu(g) * u with g = (Wg Xq)[m, n], u = (Wu Xq)[m, n],
+ * silu(g) = g / (1 + exp(-g)).
+ * Wg, Wu: N x K repacked q4_0; H: M x N fp32. */
+int bqg_gemv_q4_0_q8_1_gate_up_swiglu(const void *Wg, const void *Wu, const void *Xq, float *H,
+                                      int M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream);
+
+/* Prefill GEMM ("llama-3x-prompt-speed", "the tile"): each weight tile is
+ * dequantized once to bf16 ((q-8)*d rounded to nearest-even bf16) in shared
+ * memory and fed to the tensor cores with fp32 accumulation.
+ * Wp: repacked q4_0 N x K; X: M x K bf16; Y: M x N fp32.
+ * M a positive multiple of 128, N a multiple of 128, K a multiple of 64. */
+int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
+                       void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Debug export: the exact per-block integer dots of q4_0 x q8_1 for one
+ * activation row, computed by the same device routine as the GEMV.
+ * dots: N x K/32 int32, row-major (4-byte alignment is enough). */
+int bqg_debug_q4_0_q8_1_block_dots(const void *Wp, const void *Xq, int32_t *dots, int64_t N,
+                                   int64_t K, cudaStream_t stream);
+
+/* ---- utilities -------------------------------------------------------- */
+
+/* Workspace bytes that op needs for this shape on the current device
+ * (0 = none).  For BQG_OP_QKV_Q4_0_Q8_1 pass N = Nq + 2*Nkv. */
+size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K);
+
+/* Reads and clears this device's error word, which a bounded device-side
+ * wait sets when it gives up (0 = none).  Synchronizes `stream` first.
+ * Returns BQG_OK or BQG_ERR_CUDA; *out receives the word. */
+int bqg_last_device_error(cudaStream_t stream, int *out);
+
+/* Programmatic dependent launch for the GEMV kernels (default off).
+ * When on, a GEMV may start and prefetch its weights into L2 while the
+ * previous kernel on the stream finishes; it waits for that kernel before
+ * reading X or writing Y.  Weights must not be written by a kernel that is
+ * still running when the GEMV is enqueued.  Returns the previous setting. */
+int bqg_set_pdl(int enable);
+
+/* Static description of a status code. */
+const char *bqg_status_string(int status);
+
+/* Library version, e.g. "bqgemv 0.1 sm_103a". */
+const char *bqg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BQGEMV_H */
