@@ -43,6 +43,7 @@ EXPORTS = {
     "bqg_set_pdl": (["i"], "i"),
     "bqg_status_string": (["i"], "str"),
     "bqg_version": ([], "str"),
+    "bqg_last_cuda_error": ([], "str"),
 }
 _CT = {"i": ctypes.c_int, "i64": ctypes.c_int64, "p": ctypes.c_void_p, "size": ctypes.c_size_t,
        "str": ctypes.c_char_p}
@@ -54,7 +55,8 @@ _lib = None
 class BqgError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        detail = f" [{load().bqg_last_cuda_error().decode()}]" if status == 5 else ""
+        super().__init__(f"{where}: {status_string(status)} (status {status}){detail}")
 
 
 def load(path: str | None = None) -> ctypes.CDLL:

@@ -14,6 +14,10 @@ cudaError_t gemv_run_bf16(const GemvParams &, int, int, dim3, int, size_t, cudaS
 cudaError_t gemv_run_q8_0(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_run_q4_0(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_run_q4_0_q8_1(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_error_bf16(int *);
+cudaError_t gemv_error_q8_0(int *);
+cudaError_t gemv_error_q4_0(int *);
+cudaError_t gemv_error_q4_0_q8_1(int *);
 cudaError_t launch_quantize_q8_1(const void *, int, void *, int, int64_t, cudaStream_t, bool);
 cudaError_t launch_quantize_weights(int, const float *, void *, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_repack(int, const void *, void *, int64_t, int64_t, cudaStream_t);
@@ -29,6 +33,15 @@ using namespace bqg;
 namespace {
 
 std::atomic<int> g_pdl{0};
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return BQG_OK;
+    t_last_cuda = e;
+    return BQG_ERR_CUDA;
+}
+
 
 struct DevInfo {
     bool init = false;
@@ -93,13 +106,22 @@ RunFn runner(int wf, int xf)
 }
 
 struct GemvPlan {
-    int C, TPR, RG, RB, nc, cps, splits, threads;
-    int64_t rows_per_cta;
+    int C, TPR, RG, RPS, nc, cps, splits, threads, ncons, S, NS, stride, win_stages, part_off, bar_off, ctas;
     dim3 grid;
     size_t smem, ws_bytes;
 };
 
 constexpr int kMaxK = 65536;
+constexpr int kStageBudget = 110 * 1024;   // bytes of staged weights per CTA (two CTAs fit an SM)
+
+// Bytes of a row holding chunks [0, cps) in the repacked layout.
+int64_t range_bytes(int wf, int cps)
+{
+    if (wf == W_BF16) return 16ll * cps;
+    const int per_tile = (wf == W_Q8_0) ? 64 : 32;
+    const int64_t tb = (wf == W_Q8_0) ? Q8_0_TILE : Q4_0_TILE;
+    return (int64_t)((cps + per_tile - 1) / per_tile) * tb;
+}
 
 // Launch geometry for Nv virtual rows.  `unit` = 2 keeps (gate, up) pairs
 // in one CTA.  Returns a status.
@@ -108,28 +130,42 @@ int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevI
 {
     GemvPlan g{};
     g.nc = chunk_space(wf, K);
-    g.RB = (M == 1) ? 8 : (M == 2) ? 4 : 2;
-    // Split K only when there are too few row batches to give every SM one.
+    g.RPS = (M == 8) ? 1 : 4 / M;
+    const int align = (wf == W_Q8_0) ? 64 : 32;        // splits start on whole tiles
+    const int maxs = std::max(1, std::min(16, g.nc / std::max(align, 64)));
+    // Split K when there are too few rows to give every SM a few stages of
+    // work, or when a staged row would not leave room for two stages.
     g.splits = 1;
-    const int64_t batches = (Nv + g.RB - 1) / g.RB;
-    if (batches < dev.sms) {
-        const int want = (int)((dev.sms + batches - 1) / batches);
-        const int maxs = std::max(1, g.nc / 64);
-        g.splits = std::max(1, std::min(std::min(want, maxs), 16));
+    if (Nv < (int64_t)dev.sms * 4)
+        g.splits = (int)std::min<int64_t>(maxs, ((int64_t)dev.sms * 4 + Nv - 1) / std::max<int64_t>(Nv, 1));
+    for (;;) {
+        g.cps = g.nc;
+        if (g.splits > 1) {
+            g.cps = ((g.nc + g.splits - 1) / g.splits + align - 1) / align * align;
+            g.splits = (g.nc + g.cps - 1) / g.cps;
+        }
+        g.C = 1;
+        while ((g.cps + g.C - 1) / g.C > 512 && g.C < 4) g.C *= 2;
+        g.TPR = ((g.cps + g.C - 1) / g.C + 31) / 32 * 32;
+        g.RG = std::max(1, std::min(8, 512 / g.TPR));
+        g.S = g.RG * g.RPS;
+        g.stride = (int)range_bytes(wf, g.cps);
+        const bool fits = (g.cps + g.C - 1) / g.C <= 512 && 2ll * g.S * g.stride <= 2 * kStageBudget;
+        if (fits) break;
+        if (g.splits >= maxs) return BQG_ERR_UNSUPPORTED_SHAPE;
+        g.splits++;
     }
-    g.cps = g.nc;
-    if (g.splits > 1) {
-        g.cps = ((g.nc + g.splits - 1) / g.splits + 31) / 32 * 32;
-        g.splits = (g.nc + g.cps - 1) / g.cps;
-    }
-    g.C = 1;
-    while ((g.cps + g.C - 1) / g.C > 512 && g.C < 4) g.C *= 2;
-    if ((g.cps + g.C - 1) / g.C > 512) return BQG_ERR_UNSUPPORTED_SHAPE;
-    g.TPR = ((g.cps + g.C - 1) / g.C + 31) / 32 * 32;
-    g.RG = std::max(1, std::min(8, 512 / g.TPR));
-    g.threads = g.RG * g.TPR;
-    const int WPG = g.TPR / 32, V = g.RB * M;
-    g.smem = (WPG > 1) ? (size_t)g.RG * 2 * V * WPG * sizeof(float) : 0;
+    g.ncons = g.RG * g.TPR;
+    g.threads = g.ncons + 32;
+    g.NS = (int)std::max<int64_t>(2, std::min<int64_t>(8, kStageBudget / ((int64_t)g.S * g.stride)));
+    const int WPG = g.TPR / 32;
+    g.win_stages = std::max(1, (64 + g.S - 1) / g.S);
+    if (unit == 2 && (g.win_stages * g.S) % 2) g.win_stages *= 2;
+    g.part_off = g.NS * g.S * g.stride;
+    const int part_bytes = g.win_stages * g.S * WPG * M * (int)sizeof(float);
+    g.bar_off = (g.part_off + part_bytes + 15) / 16 * 16;
+    g.smem = (size_t)g.bar_off + 16 * g.NS;
+    if (g.smem > 232448) return BQG_ERR_UNSUPPORTED_SHAPE;
 
     int bpsm = 0;
     {
@@ -141,26 +177,23 @@ int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevI
         } else {
             lk.unlock();
             GemvParams dummy{};
-            if (runner(wf, xf)(dummy, M, g.C, dim3(1), g.threads, g.smem, 0, false, &bpsm) != cudaSuccess)
-                return BQG_ERR_CUDA;
+            const cudaError_t e = runner(wf, xf)(dummy, M, g.C, dim3(1), g.threads, g.smem, 0, false, &bpsm);
+            if (e != cudaSuccess) return cuda_status(e);
             lk.lock();
             g_occ[key] = bpsm;
         }
     }
-    bpsm = std::max(1, bpsm);
-    const int64_t slots = (int64_t)dev.sms * bpsm;
-    int64_t rpc = (Nv * g.splits + slots - 1) / slots;
-    if (unit == 2) rpc = (rpc + 1) / 2 * 2;
-    g.rows_per_cta = std::max<int64_t>(rpc, unit);
-    const int64_t gx = (Nv + g.rows_per_cta - 1) / g.rows_per_cta;
-    if (gx > 0x7fffffff) return BQG_ERR_UNSUPPORTED_SHAPE;
-    g.grid = dim3((unsigned)gx, (unsigned)g.splits);
+    if (bpsm < 1) return BQG_ERR_UNSUPPORTED_SHAPE;
+    bpsm = std::min(bpsm, 2);
+    const int64_t units = Nv / unit;
+    const int64_t want = ((int64_t)dev.sms * bpsm + g.splits - 1) / g.splits;
+    g.ctas = (int)std::max<int64_t>(1, std::min(units, want));
+    g.grid = dim3((unsigned)g.ctas, (unsigned)g.splits);
     g.ws_bytes = (g.splits > 1) ? (size_t)g.splits * M * Nv * sizeof(float) : 0;
     *pl = g;
     return BQG_OK;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? BQG_OK : BQG_ERR_CUDA; }
 
 // Common path of every GEMV entry point.
 int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void *ws, size_t ws_bytes,
@@ -185,17 +218,23 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     p.nc = g.nc;
     p.TPR = g.TPR;
     p.RG = g.RG;
-    p.rows_per_cta = g.rows_per_cta;
     p.chunks_per_split = g.cps;
+    p.nstages = g.NS;
+    p.stage_rows = g.S;
+    p.row_stride = g.stride;
+    p.win_stages = g.win_stages;
+    p.part_off = g.part_off;
+    p.bar_off = g.bar_off;
+    p.ctas = g.ctas;
     p.ws = (float *)ws;
     p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;
     const bool pdl = g_pdl.load() != 0;
-    p.prefetch_rows = pdl ? 8 : 0;
+    p.prefetch_rows = pdl ? g.NS * g.S : 0;
     cudaError_t e = runner(wf, xf)(p, M, g.C, g.grid, g.threads, g.smem, stream, pdl, nullptr);
-    if (e != cudaSuccess) return BQG_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
     if (g.splits > 1) {
         e = launch_splitk_reduce(p, M, g.splits, final_epi, stream, pdl);
-        if (e != cudaSuccess) return BQG_ERR_CUDA;
+        if (e != cudaSuccess) return cuda_status(e);
     }
     return BQG_OK;
 }
@@ -245,6 +284,8 @@ const char *bqg_status_string(int s)
 }
 
 const char *bqg_version(void) { return "bqgemv 0.1 sm_103a"; }
+
+const char *bqg_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda); }
 
 int bqg_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
@@ -401,7 +442,15 @@ size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K)
 int bqg_last_device_error(cudaStream_t stream, int *out)
 {
     if (!out) return BQG_ERR_INVALID_ARG;
-    return gemm_read_error(stream, out);
+    int word = 0;
+    if (int st = gemm_read_error(stream, &word)) return st;
+    int w = 0;
+    for (auto fn : {gemv_error_bf16, gemv_error_q8_0, gemv_error_q4_0, gemv_error_q4_0_q8_1}) {
+        if (fn(&w) != cudaSuccess) return BQG_ERR_CUDA;
+        word |= w;
+    }
+    *out = word;
+    return BQG_OK;
 }
 
 }  // extern "C"

@@ -59,7 +59,18 @@ struct GemvParams {
     int64_t rows_per_cta;   // virtual rows per CTA (multiple of 2 for gate/up)
     int chunks_per_split;   // chunk range of one split (grid.y)
     int prefetch_rows;      // rows of this CTA to warm in L2 before griddepcontrol.wait
+    // shared-memory pipeline
+    int nstages;            // NS stages in the ring
+    int stage_rows;         // S rows per stage (RG * rows per group per stage)
+    int row_stride;         // bytes of one staged row (largest split range, multiple of 16)
+    int win_stages;         // stages per partial-sum window
+    int part_off;           // byte offset of the partial sums
+    int bar_off;            // byte offset of the mbarriers (8-byte aligned)
+    int ctas;               // CTAs along grid.x (rows are split evenly over them)
 };
+
+// Error word set when a bounded wait gives up (one per translation unit).
+static __device__ int g_gemv_error;
 
 // Virtual row -> (matrix, row in matrix)
 __device__ __forceinline__ void map_row(const GemvParams &p, int64_t v, int &mat, int64_t &r)
@@ -173,6 +184,27 @@ __device__ __forceinline__ void load_w(WChunk<WF> &w, const uint8_t *row, int c,
     else w.s = 0;
 }
 
+// Chunk c from a row staged in shared memory starting at byte `base` of the row.
+template <int WF>
+__device__ __forceinline__ void lds_w(WChunk<WF> &w, const uint8_t *srow, int64_t base, int c)
+{
+    w.c = *reinterpret_cast<const uint4 *>(srow + (chunk_code_off<WF>(c) - base));
+    if constexpr (WF != W_BF16) w.s = *reinterpret_cast<const uint16_t *>(srow + (chunk_scale_off<WF>(c) - base));
+    else w.s = 0;
+}
+
+// Byte range [off, off + bytes) of a row that holds chunks [cbeg, cend).
+template <int WF>
+__device__ __host__ __forceinline__ void chunk_range_bytes(int cbeg, int cend, int64_t &off, int64_t &bytes)
+{
+    if (WF == W_BF16) { off = 16ll * cbeg; bytes = 16ll * (cend - cbeg); return; }
+    const int per_tile = (WF == W_Q8_0) ? 64 : 32;
+    const int64_t tb = (WF == W_Q8_0) ? Q8_0_TILE : Q4_0_TILE;
+    const int64_t t0 = cbeg / per_tile, t1 = (cend + per_tile - 1) / per_tile;
+    off = t0 * tb;
+    bytes = (t1 - t0) * tb;
+}
+
 // Exact per-block integer dot of a q4_0 code chunk with a q8_1 block:
 // sum_i (qw_i - 8) qx_i.  Word i of the codes holds elements 4i..4i+3 in its
 // low nibbles and 16+4i..16+4i+3 in its high nibbles; x.q[i] holds codes
@@ -244,32 +276,111 @@ __device__ __forceinline__ void named_barrier(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// rows in flight per thread for each M (RB * M values are reduced per batch)
-template <int M> struct RowsPerBatch { static constexpr int value = (M == 1) ? 8 : (M == 2) ? 4 : 2; };
+// rows each group takes from a stage; V = RPS * M values per warp reduction
+template <int M> struct RowsPerStage { static constexpr int value = (M == 8) ? 1 : 4 / M; };
+
+// This CTA's virtual rows [v0, v1): an even split of Nv over p.ctas CTAs
+// (in pairs when gate and up rows alternate).
+__device__ __forceinline__ void cta_rows(const GemvParams &p, int64_t &v0, int64_t &v1)
+{
+    const int64_t unit = (p.nmat == 2) ? 2 : 1;
+    const int64_t units = p.Nv / unit;
+    v0 = (int64_t)blockIdx.x * units / p.ctas * unit;
+    v1 = (int64_t)(blockIdx.x + 1) * units / p.ctas * unit;
+}
 
 // ---------------------------------------------------------------------------
-// the kernel
+// the kernel: one producer warp streams the CTA's rows into a ring of
+// shared-memory stages with cp.async.bulk; RG x TPR consumer threads read
+// their K-slice of each staged row against activations held in registers.
+// Per-row partial sums of each warp go to shared memory and are combined
+// (in warp order, so results are deterministic) once per window of rows.
+// Every wait on an mbarrier is bounded; on a timeout the kernel records an
+// error in g_gemv_error and finishes without reading stale data.
 // ---------------------------------------------------------------------------
 template <int WF, int XF, int M, int C>
-__global__ void __launch_bounds__(512) gemv_kernel(const GemvParams p)
+__global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvParams p)
 {
-    constexpr int RB = RowsPerBatch<M>::value;
-    constexpr int V = RB * M;
+    constexpr int RPS = RowsPerStage<M>::value;
+    constexpr int V = RPS * M;
     using WR = WarpReduce<V>;
-    extern __shared__ float sred[];        // [RG][2][V][WPG] when a group has > 1 warp
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_abort;
 
     const int tid = threadIdx.x;
-    const int g = tid / p.TPR;             // row group
-    const int tau = tid - g * p.TPR;       // thread in group
     const int lane = tid & 31;
-    const int wig = tau >> 5;              // warp in group
-    const int WPG = p.TPR >> 5;
+    const int ncons = p.RG * p.TPR;                // consumer threads (a multiple of 32)
+    const int S = p.stage_rows;
+    const int NS = p.nstages;
+    uint8_t *stages = smem;
+    float *part = reinterpret_cast<float *>(smem + p.part_off);
+    const uint32_t bar0 = smem_u32(smem + p.bar_off);   // full[NS] then empty[NS]
 
-    const int64_t v0 = (int64_t)blockIdx.x * p.rows_per_cta;
-    const int64_t v1 = min(p.Nv, v0 + p.rows_per_cta);
+    int64_t v0, v1;
+    cta_rows(p, v0, v1);
     const int split = blockIdx.y;
     const int cbeg = split * p.chunks_per_split;
     const int cend = min(p.nc, cbeg + p.chunks_per_split);
+    int64_t roff, rbytes;
+    chunk_range_bytes<WF>(cbeg, cend, roff, rbytes);
+    const int64_t nst = (v1 - v0 + S - 1) / S;      // stages this CTA streams
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; i++) {
+            mbar_init(bar0 + 8 * i, 1);                       // full: producer's arrive + bytes
+            mbar_init(bar0 + 8 * (NS + i), ncons / 32);       // empty: one arrive per consumer warp
+        }
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (tid >= ncons) {
+        // ---------------- producer warp ----------------
+        if (lane != 0) return;
+        if (p.prefetch_rows > 0) {          // warm L2 before the previous grid ends
+            const int64_t npf = min((int64_t)p.prefetch_rows, v1 - v0);
+            for (int64_t j = 0; j < npf; j++) {
+                int mat; int64_t rr;
+                map_row(p, v0 + j, mat, rr);
+                prefetch_l2_bulk(p.W[mat] + rr * p.row_bytes + roff, (uint32_t)rbytes);
+            }
+        }
+        pdl_wait();
+        pdl_launch_dependents();
+        int64_t issued = 0;
+        for (int64_t j = 0; j < nst; j++) {
+            const int s = (int)(j % NS);
+            if (j >= NS && !mbar_wait_bounded(bar0 + 8 * (NS + s), (uint32_t)(((j / NS) - 1) & 1))) {
+                atomicExch(&g_gemv_error, 1);
+                s_abort = 1;
+                break;
+            }
+            if (*(volatile int *)&s_abort) break;
+            const int64_t vs = v0 + j * S;
+            const int nrow = (int)min((int64_t)S, v1 - vs);
+            mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(nrow * rbytes));
+            const uint32_t dst = smem_u32(stages) + (uint32_t)s * (uint32_t)(S * p.row_stride);
+            for (int r = 0; r < nrow; r++) {
+                int mat; int64_t rr;
+                map_row(p, vs + r, mat, rr);
+                bulk_g2s(dst + r * p.row_stride, p.W[mat] + rr * p.row_bytes + roff, (uint32_t)rbytes, bar0 + 8 * s);
+            }
+            issued = j + 1;
+        }
+        // do not leave while copies into this CTA's shared memory are in flight
+        for (int64_t j = max((int64_t)0, issued - NS); j < issued; j++)
+            mbar_wait_bounded(bar0 + 8 * (int)(j % NS), (uint32_t)((j / NS) & 1));
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    pdl_wait();
+    pdl_launch_dependents();
+    const int g = tid / p.TPR;             // row group
+    const int tau = tid - g * p.TPR;       // thread in group
+    const int wig = tau >> 5;              // warp in group
+    const int WPG = p.TPR >> 5;
 
     int cid[C];
     bool cval[C];
@@ -278,110 +389,88 @@ __global__ void __launch_bounds__(512) gemv_kernel(const GemvParams p)
         cid[i] = cbeg + tau + i * p.TPR;
         cval[i] = cid[i] < cend && chunk_valid<WF>(cid[i], p.nb, p.nc);
     }
-
-    // Before waiting for the previous grid: warm L2 with the first rows of
-    // this CTA (weights do not depend on that grid; nothing is consumed).
-    if (p.prefetch_rows > 0) {
-        const int64_t npf = min((int64_t)p.prefetch_rows, v1 - v0);
-        for (int64_t j = tid; j < npf; j += blockDim.x) {
-            int mat; int64_t rr;
-            map_row(p, v0 + j, mat, rr);
-            prefetch_l2_bulk(p.W[mat] + rr * p.row_bytes, (uint32_t)p.row_bytes);
-        }
-    }
-    pdl_wait();
-    pdl_launch_dependents();
-
     XSlice<WF, XF> xs[C][M];
 #pragma unroll
     for (int i = 0; i < C; i++)
 #pragma unroll
         for (int m = 0; m < M; m++) load_x<WF, XF>(xs[i][m], p, m, cid[i], cval[i]);
 
-    // Group g visits units g, g + RG, g + 2 RG, ... of this CTA's rows; a unit
-    // is one row, or a (gate, up) row pair for the SwiGLU epilogue.  RB rows
-    // (RB / U units) are in flight per thread.
-    const int U = (p.epi == EPI_SWIGLU || p.nmat == 2) ? 2 : 1;
-    auto row_of = [&](int64_t i0, int r) -> int64_t {
-        return v0 + (g + (int64_t)p.RG * (i0 + r / U)) * U + (r % U);
-    };
-    WChunk<WF> wc[RB][C];
-    int64_t i0 = 0;
-    const int64_t di = RB / U;
-    if (row_of(0, 0) < v1) {
-#pragma unroll
-        for (int r = 0; r < RB; r++) {
-            const int64_t v = row_of(0, r);
-            const bool rv = v < v1;
-            const uint8_t *row = nullptr;
-            if (rv) { int mat; int64_t rr; map_row(p, v, mat, rr); row = p.W[mat] + rr * p.row_bytes; }
-#pragma unroll
-            for (int i = 0; i < C; i++) load_w<WF>(wc[r][i], row, cid[i], rv && cval[i]);
+    const int64_t WIN = (int64_t)p.win_stages * S;
+    int64_t win0 = v0;
+    bool ok = true;
+    for (int64_t j = 0; j < nst; j++) {
+        const int s = (int)(j % NS);
+        if (ok && !mbar_wait_bounded(bar0 + 8 * s, (uint32_t)((j / NS) & 1))) {
+            atomicExch(&g_gemv_error, 1);
+            s_abort = 1;
         }
-    }
-    int buf = 0;
-    for (; row_of(i0, 0) < v1; i0 += di) {
+        ok = ok && !*(volatile int *)&s_abort;
+        const int64_t vs = v0 + j * S;
+        const uint8_t *stage = stages + (size_t)s * S * p.row_stride;
         float acc[V];
 #pragma unroll
-        for (int r = 0; r < RB; r++)
+        for (int rr = 0; rr < RPS; rr++) {
+            const int r = g + p.RG * rr;
+            const bool rv = ok && (vs + r < v1);
+            const uint8_t *srow = stage + (size_t)r * p.row_stride;
+            WChunk<WF> wc[C];
+#pragma unroll
+            for (int i = 0; i < C; i++) {
+                if (rv && cval[i]) lds_w<WF>(wc[i], srow, roff, cid[i]);
+                else { wc[i].c = make_uint4(0, 0, 0, 0); wc[i].s = 0; }
+            }
 #pragma unroll
             for (int m = 0; m < M; m++) {
                 float a = 0.f;
 #pragma unroll
-                for (int i = 0; i < C; i++) a += chunk_dot<WF, XF>(wc[r][i], xs[i][m]);
-                acc[r * M + m] = a;
+                for (int i = 0; i < C; i++) a += chunk_dot<WF, XF>(wc[i], xs[i][m]);
+                acc[rr * M + m] = a;
             }
-        // issue the next batch before reducing this one
-        if (row_of(i0 + di, 0) < v1) {
-#pragma unroll
-            for (int r = 0; r < RB; r++) {
-                const int64_t v = row_of(i0 + di, r);
-                const bool rv = v < v1;
-                const uint8_t *row = nullptr;
-                if (rv) { int mat; int64_t rr; map_row(p, v, mat, rr); row = p.W[mat] + rr * p.row_bytes; }
-#pragma unroll
-                for (int i = 0; i < C; i++) load_w<WF>(wc[r][i], row, cid[i], rv && cval[i]);
-            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar0 + 8 * (NS + s));     // this warp is done with stage s
+
+        const float tot = WR::run(acc, lane);
+        if (WR::is_holder(lane)) {
+            const int idx = WR::index_of_lane(lane);
+            const int rr = idx / M, m = idx - (idx / M) * M;
+            const int64_t v = vs + g + (int64_t)p.RG * rr;
+            if (v < v1) part[((v - win0) * WPG + wig) * M + m] = tot;
         }
 
-        float tot = WR::run(acc, lane);
-        int idx = WR::index_of_lane(lane);
-        bool holder = WR::is_holder(lane);
-        bool finals_here = true;            // does this warp hold the finished sums?
-        if (WPG > 1) {
-            float *slot = sred + (size_t)(g * 2 + buf) * V * WPG;
-            if (holder) slot[idx * WPG + wig] = tot;
-            named_barrier(1 + g, p.TPR);
-            finals_here = (wig == 0);
-            if (finals_here) {
-                float s = 0.f;
-                if (lane < V)
-                    for (int w = 0; w < WPG; w++) s += slot[lane * WPG + w];
-                tot = s;
-                idx = lane;
-                holder = lane < V;
-            }
-            buf ^= 1;
-        }
-        if (finals_here) {
-            const int r = idx / M, m = idx - (idx / M) * M;
-            const int64_t v = row_of(i0, r);
+        // window complete: combine the warps' partials (warp order) and store
+        if ((j + 1) % p.win_stages == 0 || j + 1 == nst) {
+            named_barrier(1, ncons);
+            const int64_t nrw = min(WIN, v1 - win0);
             if (p.epi == EPI_SWIGLU) {
-                // (gate, up) rows alternate; batches start on even rows
-                const int pidx = min(idx + M, V - 1);
-                const int plane = (WPG > 1) ? pidx : WR::lane_of_index(pidx);
-                const float u = __shfl_sync(0xffffffffu, tot, plane);
-                if (holder && (r & 1) == 0 && v < v1)
-                    p.Y[0][(int64_t)m * p.rows[0] + (v >> 1)] = silu(tot) * u;
-            } else if (p.epi == EPI_PARTIAL) {
-                if (holder && v < v1) p.ws[((int64_t)split * M + m) * p.Nv + v] = tot;
+                for (int64_t t = tid; t < (nrw >> 1) * M; t += ncons) {
+                    const int64_t pr = t / M;
+                    const int m = (int)(t - pr * M);
+                    float gs = 0.f, us = 0.f;
+                    for (int w = 0; w < WPG; w++) {
+                        gs += part[((2 * pr) * WPG + w) * M + m];
+                        us += part[((2 * pr + 1) * WPG + w) * M + m];
+                    }
+                    p.Y[0][(int64_t)m * p.rows[0] + ((win0 >> 1) + pr)] = silu(gs) * us;
+                }
             } else {
-                if (holder && v < v1) {
-                    int mat; int64_t rr;
-                    map_row(p, v, mat, rr);
-                    p.Y[mat][(int64_t)m * p.rows[mat] + rr] = tot;
+                for (int64_t t = tid; t < nrw * M; t += ncons) {
+                    const int64_t row = t / M;
+                    const int m = (int)(t - row * M);
+                    float sum = 0.f;
+                    for (int w = 0; w < WPG; w++) sum += part[(row * WPG + w) * M + m];
+                    const int64_t v = win0 + row;
+                    if (p.epi == EPI_PARTIAL) {
+                        p.ws[((int64_t)split * M + m) * p.Nv + v] = sum;
+                    } else {
+                        int mat; int64_t rr;
+                        map_row(p, v, mat, rr);
+                        p.Y[mat][(int64_t)m * p.rows[mat] + rr] = sum;
+                    }
                 }
             }
+            named_barrier(1, ncons);
+            win0 += WIN;
         }
     }
 }
@@ -423,10 +512,16 @@ __host__ cudaError_t gemv_launch_one(const GemvParams &p, dim3 grid, int threads
 {
     auto kern = gemv_kernel<WF, XF, M, C>;
     if (occupancy) {
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-        }
+        // allow the largest dynamic shared memory (opt-in limit minus static), then ask for this size
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+        if (e == cudaSuccess && smem + fa.sharedSizeBytes > (size_t)optin) return cudaErrorInvalidValue;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+        if (e != cudaSuccess) return e;
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, threads, smem);
     }
     cudaLaunchConfig_t cfg = {};
@@ -440,6 +535,16 @@ __host__ cudaError_t gemv_launch_one(const GemvParams &p, dim3 grid, int threads
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Reads and clears this translation unit's error word.
+__host__ inline cudaError_t gemv_take_error(int *out)
+{
+    int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    *out = v;
+    return v ? cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(int)) : cudaSuccess;
 }
 
 template <int WF, int XF>

@@ -63,9 +63,10 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
     uint8_t *out = xq + blk * Q8_1_BYTES;
     out[4 + lane] = (uint8_t)(int8_t)q;
     if (lane == 0) {
+        // d | s as one little-endian word (blocks are 4-byte aligned)
         const __half sh = __float2half_rn(d * (float)sum);   // exact product, one rounding
-        const uint16_t db = __half_as_ushort(dh), sb = __half_as_ushort(sh);
-        out[0] = db & 0xff; out[1] = db >> 8; out[2] = sb & 0xff; out[3] = sb >> 8;
+        const uint32_t db = __half_as_ushort(dh), sb = __half_as_ushort(sh);
+        *reinterpret_cast<uint32_t *>(out) = db | (sb << 16);
     }
 }
 
@@ -85,10 +86,7 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(const float *__re
         const int q = q8_code(v, __half2float(dh));
         uint8_t *out = dst + blk * Q8_0_BYTES;
         out[2 + lane] = (uint8_t)(int8_t)q;
-        if (lane == 0) {
-            const uint16_t db = __half_as_ushort(dh);
-            out[0] = db & 0xff; out[1] = db >> 8;
-        }
+        if (lane == 0) *reinterpret_cast<uint16_t *>(out) = __half_as_ushort(dh);
     } else {
         // signed element of largest magnitude, lowest lane on ties
         float bv = v, ba = fabsf(v);
@@ -107,10 +105,7 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(const float *__re
         const int qhi = __shfl_down_sync(0xffffffffu, q, 16);
         uint8_t *out = dst + blk * Q4_0_BYTES;
         if (lane < 16) out[2 + lane] = (uint8_t)(q | (qhi << 4));
-        if (lane == 0) {
-            const uint16_t db = __half_as_ushort(dh);
-            out[0] = db & 0xff; out[1] = db >> 8;
-        }
+        if (lane == 0) *reinterpret_cast<uint16_t *>(out) = __half_as_ushort(dh);
     }
 }
 

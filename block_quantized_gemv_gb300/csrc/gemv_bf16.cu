@@ -7,4 +7,5 @@ cudaError_t gemv_run_bf16(const GemvParams &p, int M, int C, dim3 grid, int thre
 {
     return gemv_dispatch<W_BF16, X_BF16>(p, M, C, grid, threads, smem, stream, pdl, occupancy);
 }
+cudaError_t gemv_error_bf16(int *out) { return gemv_take_error(out); }
 }  // namespace bqg

@@ -7,4 +7,5 @@ cudaError_t gemv_run_q4_0(const GemvParams &p, int M, int C, dim3 grid, int thre
 {
     return gemv_dispatch<W_Q4_0, X_BF16>(p, M, C, grid, threads, smem, stream, pdl, occupancy);
 }
+cudaError_t gemv_error_q4_0(int *out) { return gemv_take_error(out); }
 }  // namespace bqg

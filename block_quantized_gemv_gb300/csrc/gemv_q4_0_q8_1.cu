@@ -7,4 +7,5 @@ cudaError_t gemv_run_q4_0_q8_1(const GemvParams &p, int M, int C, dim3 grid, int
 {
     return gemv_dispatch<W_Q4_0, X_Q8_1>(p, M, C, grid, threads, smem, stream, pdl, occupancy);
 }
+cudaError_t gemv_error_q4_0_q8_1(int *out) { return gemv_take_error(out); }
 }  // namespace bqg

@@ -183,6 +183,10 @@ int bqg_last_device_error(cudaStream_t stream, int *out);
  * still running when the GEMV is enqueued.  Returns the previous setting. */
 int bqg_set_pdl(int enable);
 
+/* Name of the CUDA error behind the calling thread's last BQG_ERR_CUDA
+ * ("no error" if there was none). */
+const char *bqg_last_cuda_error(void);
+
 /* Static description of a status code. */
 const char *bqg_status_string(int status);
 
