@@ -160,7 +160,7 @@ class Arm:
 
 
 class GemvArm(Arm):
-    def __init__(self, fmt, xfmt, M, N, K, seed=1):
+    def __init__(self, fmt, xfmt, M, N, K, seed=1, sets=None):
         import torch
         import block_quantized_gemv_gb300 as bqg
         from block_quantized_gemv_gb300 import synth
@@ -185,7 +185,7 @@ class GemvArm(Arm):
         self.x_bytes = X.numel() * X.element_size()
         self.y_bytes = M * N * 4
         self.bytes_per_call = self.w_bytes + self.x_bytes + self.y_bytes
-        self.R = self.rotation(self.bytes_per_call)
+        self.R = sets or self.rotation(self.bytes_per_call)
         self.fn = {bqg.BF16: bqg.gemv_bf16, bqg.Q8_0: bqg.gemv_q8_0, bqg.Q4_0: bqg.gemv_q4_0}[fmt]
         if xfmt == bqg.Q8_1:
             self.fn = bqg.gemv_q4_0_q8_1
@@ -410,6 +410,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--json-out", default=None)
+    ap.add_argument("--min-warm-s", type=float, default=1.0, help="minimum warm-up time per arm")
+    ap.add_argument("--profile", default=None, choices=["bf16", "q8_0", "q4_0", "q4_0_q8_1"],
+                    help="profiling case: only this M=1 K=4096 N=12288 arm, 2 weight sets, eager calls")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -461,10 +464,23 @@ def main():
         pass
     sampler = NvmlSampler(uuid)
 
+    if args.profile:
+        # a small case for ncu: two weight sets (cache state is ncu's to control)
+        fmt = {"bf16": bqg.BF16, "q8_0": bqg.Q8_0, "q4_0": bqg.Q4_0, "q4_0_q8_1": bqg.Q4_0}[args.profile]
+        xf = bqg.Q8_1 if args.profile == "q4_0_q8_1" else bqg.BF16
+        arm = GemvArm(fmt, xf, 1, N_HEAD, K_HEAD, sets=2)
+        for i in range(args.warmup + args.steps):
+            arm.call(i)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": arm.name, "calls": args.warmup + args.steps}))
+        return 0
+
     head = GemvArm(bqg.BF16, bqg.BF16, 1, N_HEAD, K_HEAD)
-    t = time_arm(head, args.steps, args.warmup, use_graph=not args.no_graph, sampler=sampler, dist=dist)
+    t = time_arm(head, args.steps, args.warmup, use_graph=not args.no_graph, min_warm_s=args.min_warm_s,
+                 sampler=sampler, dist=dist)
     if not t["spread_ok"]:       # protocol: reject and measure once more
-        t2 = time_arm(head, args.steps, args.warmup, use_graph=not args.no_graph, sampler=sampler, dist=dist)
+        t2 = time_arm(head, args.steps, args.warmup, use_graph=not args.no_graph, min_warm_s=args.min_warm_s,
+                      sampler=sampler, dist=dist)
         t2["first_attempt_spread"] = t["spread"]
         t = t2
     rec = arm_record(head, t, peaks)
@@ -487,8 +503,8 @@ def main():
                 other.append(GemvArm(f, bqg.BF16, M, 14336, 4096))
             other.append(GemvArm(bqg.Q4_0, bqg.Q8_1, M, 14336, 4096))
     for a in other:
-        ta = time_arm(a, args.steps, max(3, args.warmup // 4), use_graph=not args.no_graph, min_warm_s=0.3,
-                      dist=dist)
+        ta = time_arm(a, args.steps, max(3, args.warmup // 4), use_graph=not args.no_graph,
+                      min_warm_s=min(0.3, args.min_warm_s), dist=dist)
         arms.append(arm_record(a, ta, peaks))
         del a
         torch.cuda.empty_cache()
