@@ -44,6 +44,8 @@ EXPORTS = {
     "bqg_status_string": (["i"], "str"),
     "bqg_version": ([], "str"),
     "bqg_last_cuda_error": ([], "str"),
+    "bqg_gemv_q4_0_q8_1_noalloc": (["p", "p", "p", "i", "i64", "i64", "p"], "i"),
+    "bqg_noalloc_scratch_bytes": ([], "size"),
 }
 _CT = {"i": ctypes.c_int, "i64": ctypes.c_int64, "p": ctypes.c_void_p, "size": ctypes.c_size_t,
        "str": ctypes.c_char_p}
@@ -184,6 +186,18 @@ def gemv_q4_0(Wp, X, N, K, out=None, ws=None, stream=None):
 def gemv_q4_0_q8_1(Wp, Xq, N, K, out=None, ws=None, stream=None):
     M = Xq.shape[0]
     return _gemv("bqg_gemv_q4_0_q8_1", Wp, Xq, N, K, M, out, ws, stream, M * row_bytes(Q8_1, K))
+
+
+def gemv_q4_0_q8_1_noalloc(Wp, Xq, N, K, out=None, stream=None):
+    """bqg_gemv_q4_0_q8_1 without a workspace argument: split-K scratch comes
+    from a fixed array inside the library (for callers that cannot allocate)."""
+    M = Xq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=Xq.device)
+    _check(load().bqg_gemv_q4_0_q8_1_noalloc(_dev(Wp, "Wp"), _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
+                                             _dev(out, "Y", torch.float32, M * N * 4), M, N, K, _stream(stream)),
+           "bqg_gemv_q4_0_q8_1_noalloc")
+    return out
 
 
 def gemv_q4_0_q8_1_qkv(Wq, Wk, Wv, Xq, Nq, Nkv, K, out=None, ws=None, stream=None):

@@ -133,6 +133,28 @@ int bqg_gemv_q4_0(const void *Wp, const void *X, float *Y, int M, int64_t N, int
 int bqg_gemv_q4_0_q8_1(const void *Wp, const void *Xq, float *Y, int M, int64_t N, int64_t K,
                        void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* No counterpart on the pages.  An allocation-free variant of
+ * bqg_gemv_q4_0_q8_1 for callers that cannot hand the library a workspace
+ * from cudaMalloc: a runtime whose device memory plan is fixed when the
+ * model loads, a decode loop in which an allocation may block or
+ * synchronize the device, or C code with no allocator of its own.  Same
+ * arguments and arithmetic as bqg_gemv_q4_0_q8_1 without the workspace:
+ * split-K partial sums go to a fixed array of bqg_noalloc_scratch_bytes()
+ * (32 KiB) inside the library, which every device that loads the library
+ * holds until the process exits.
+ *  - The first call on each device looks up the array's device address (a
+ *    synchronous runtime call); make that first call before any stream
+ *    capture.
+ *  - A shape whose split-K partials would not fit the array returns
+ *    BQG_ERR_WORKSPACE and launches nothing.
+ *  - Every call shares the array.  Nothing in it has to start at zero (a
+ *    call writes every partial sum it reads), but calls that overlap on the
+ *    GPU, on one stream or several, race on it.
+ *  - It calls no cudaMalloc, cudaFree or allocating library routine. */
+int bqg_gemv_q4_0_q8_1_noalloc(const void *Wp, const void *Xq, float *Y, int M, int64_t N, int64_t K,
+                               cudaStream_t stream);
+size_t bqg_noalloc_scratch_bytes(void);
+
 /* Q, K and V projections of one shared activation in a single launch
  * (the grouped QKV launch of "rx-6700xt-llama2-decode", Approach &
  * Methodology).  Wq: Nq x K, Wk/Wv: Nkv x K repacked q4_0;
