@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -18,6 +19,14 @@ cudaError_t gemv_error_bf16(int *);
 cudaError_t gemv_error_q8_0(int *);
 cudaError_t gemv_error_q4_0(int *);
 cudaError_t gemv_error_q4_0_q8_1(int *);
+cudaError_t gemv_lpr_run_bf16(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q8_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q4_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+int gemv_x_stage_bytes_bf16(int, int);
+int gemv_x_stage_bytes_q8_0(int, int);
+int gemv_x_stage_bytes_q4_0(int, int);
+int gemv_x_stage_bytes_q4_0_q8_1(int, int);
 cudaError_t launch_quantize_q8_1(const void *, int, void *, int, int64_t, cudaStream_t, bool);
 cudaError_t launch_quantize_weights(int, const float *, void *, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_repack(int, const void *, void *, int64_t, int64_t, cudaStream_t);
@@ -105,14 +114,54 @@ RunFn runner(int wf, int xf)
     return gemv_run_q4_0;
 }
 
+using LprFn = cudaError_t (*)(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+LprFn lpr_runner(int wf, int xf)
+{
+    if (xf == X_Q8_1) return gemv_lpr_run_q4_0_q8_1;
+    if (wf == W_BF16) return gemv_lpr_run_bf16;
+    if (wf == W_Q8_0) return gemv_lpr_run_q8_0;
+    return gemv_lpr_run_q4_0;
+}
+int x_stage_bytes(int wf, int xf, int nc, int nb)
+{
+    if (xf == X_Q8_1) return gemv_x_stage_bytes_q4_0_q8_1(nc, nb);
+    if (wf == W_BF16) return gemv_x_stage_bytes_bf16(nc, nb);
+    if (wf == W_Q8_0) return gemv_x_stage_bytes_q8_0(nc, nb);
+    return gemv_x_stage_bytes_q4_0(nc, nb);
+}
+
 struct GemvPlan {
+    bool lpr;               // lanes-per-row kernel (M <= 2)
+    int L, x_off, x_row_bytes, wg, ng;
     int C, TPR, RG, RPS, nc, cps, splits, threads, ncons, S, NS, stride, win_stages, part_off, bar_off, ctas;
     dim3 grid;
     size_t smem, ws_bytes;
 };
 
 constexpr int kMaxK = 65536;
-constexpr int kStageBudget = 110 * 1024;   // bytes of staged weights per CTA (two CTAs fit an SM)
+// Staged weights per CTA.  Two CTAs per SM stream a GEMV; when one of them
+// finishes, the next GEMV's CTA takes its place and starts its own weight
+// stream while the other drains (programmatic dependent launch).
+constexpr int kStageBudget = 100 * 1024;
+
+// Tuning knobs read once from the environment (unset = defaults above):
+//   BQG_STAGE_KB     staged-weight budget per CTA in KiB
+//   BQG_CTAS_PER_SM  cap on resident GEMV CTAs per SM (1 or 2)
+int env_int(const char *name, int dflt)
+{
+    const char *v = getenv(name);
+    return (v && *v) ? atoi(v) : dflt;
+}
+int stage_budget()
+{
+    static const int b = std::max(16, std::min(200, env_int("BQG_STAGE_KB", kStageBudget / 1024))) * 1024;
+    return b;
+}
+int ctas_per_sm_cap()
+{
+    static const int c = std::max(1, std::min(2, env_int("BQG_CTAS_PER_SM", 2)));
+    return c;
+}
 
 // Bytes of a row holding chunks [0, cps) in the repacked layout.
 int64_t range_bytes(int wf, int cps)
@@ -147,20 +196,23 @@ int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevI
         g.C = 1;
         while ((g.cps + g.C - 1) / g.C > 512 && g.C < 4) g.C *= 2;
         g.TPR = ((g.cps + g.C - 1) / g.C + 31) / 32 * 32;
-        g.RG = std::max(1, std::min(8, 512 / g.TPR));
-        g.S = g.RG * g.RPS;
+        // row groups per CTA: at most 512 consumer threads, and few enough rows
+        // per stage that at least four stages fit the budget
+        g.RG = std::max(1, std::min(std::min(8, 512 / g.TPR),
+                                    (int)(stage_budget() / (4ll * g.RPS * range_bytes(wf, g.cps)))));
+        // a stage is SUB passes of RG x RPS rows; gate/up stages need an even row count
+        g.S = g.RG * g.RPS * ((unit == 2 && (g.RG * g.RPS) % 2) ? 2 : 1);
         g.stride = (int)range_bytes(wf, g.cps);
-        const bool fits = (g.cps + g.C - 1) / g.C <= 512 && 2ll * g.S * g.stride <= 2 * kStageBudget;
+        const bool fits = (g.cps + g.C - 1) / g.C <= 512 && 2ll * g.S * g.stride <= 2 * stage_budget();
         if (fits) break;
         if (g.splits >= maxs) return BQG_ERR_UNSUPPORTED_SHAPE;
         g.splits++;
     }
     g.ncons = g.RG * g.TPR;
     g.threads = g.ncons + 32;
-    g.NS = (int)std::max<int64_t>(2, std::min<int64_t>(8, kStageBudget / ((int64_t)g.S * g.stride)));
+    g.NS = (int)std::max<int64_t>(2, std::min<int64_t>(8, stage_budget() / ((int64_t)g.S * g.stride)));
     const int WPG = g.TPR / 32;
     g.win_stages = std::max(1, (64 + g.S - 1) / g.S);
-    if (unit == 2 && (g.win_stages * g.S) % 2) g.win_stages *= 2;
     g.part_off = g.NS * g.S * g.stride;
     const int part_bytes = g.win_stages * g.S * WPG * M * (int)sizeof(float);
     g.bar_off = (g.part_off + part_bytes + 15) / 16 * 16;
@@ -184,7 +236,7 @@ int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevI
         }
     }
     if (bpsm < 1) return BQG_ERR_UNSUPPORTED_SHAPE;
-    bpsm = std::min(bpsm, 2);
+    bpsm = std::min(bpsm, ctas_per_sm_cap());
     const int64_t units = Nv / unit;
     const int64_t want = ((int64_t)dev.sms * bpsm + g.splits - 1) / g.splits;
     g.ctas = (int)std::max<int64_t>(1, std::min(units, want));
@@ -194,6 +246,96 @@ int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevI
     return BQG_OK;
 }
 
+
+// Launch geometry of the lanes-per-row kernel (M <= 2).  Returns
+// BQG_ERR_UNSUPPORTED_SHAPE when the staged activations would not fit, in
+// which case the K-slice kernel (plan_gemv) serves the call.
+int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevInfo &dev, int device,
+             GemvPlan *pl)
+{
+    if (M > 2) return BQG_ERR_UNSUPPORTED_SHAPE;
+    static const bool off = env_int("BQG_NO_LPR", 0) != 0;
+    if (off) return BQG_ERR_UNSUPPORTED_SHAPE;
+    GemvPlan g{};
+    g.lpr = true;
+    g.nc = chunk_space(wf, K);
+    const int nb = (int)(K / QK);
+    const int align = (wf == W_Q8_0) ? 64 : 32;
+    const int maxs = std::max(1, std::min(16, g.nc / std::max(align, 64)));
+    g.splits = 1;
+    if (Nv < (int64_t)dev.sms * 4)
+        g.splits = (int)std::min<int64_t>(maxs, ((int64_t)dev.sms * 4 + Nv - 1) / std::max<int64_t>(Nv, 1));
+    for (;;) {
+        g.cps = g.nc;
+        if (g.splits > 1) {
+            g.cps = ((g.nc + g.splits - 1) / g.splits + align - 1) / align * align;
+            g.splits = (g.nc + g.cps - 1) / g.cps;
+        }
+        g.stride = (int)range_bytes(wf, g.cps);
+        if (2ll * g.stride <= stage_budget()) break;
+        if (g.splits >= maxs) return BQG_ERR_UNSUPPORTED_SHAPE;
+        g.splits++;
+    }
+    // lanes per row: at least eight chunks per lane; gate/up pairs need two rows per warp
+    g.L = (g.cps >= 256) ? 32 : (g.cps >= 128) ? 16 : 8;
+    if (unit == 2 && g.L == 32) g.L = 16;
+    const int R = 32 / g.L;
+    // stages of about 16 KiB, a whole number of warps' rows
+    int rows = std::max(1, (int)(16384 / g.stride));
+    rows = std::max(R, rows / R * R);
+    g.S = rows;
+    const int wg = g.S / R;
+    g.NS = (int)std::max<int64_t>(2, std::min<int64_t>(16, stage_budget() / ((int64_t)g.S * g.stride)));
+    const int ng = std::max(1, std::min(g.NS, 16 / wg));
+    g.wg = wg;
+    g.ng = ng;
+    g.TPR = 32 * wg * ng;
+    g.RG = 1;
+    g.C = 1;
+    g.ncons = g.TPR;
+    g.threads = g.ncons + 32;
+    g.x_row_bytes = (x_stage_bytes(wf, xf, g.nc, nb) + 15) / 16 * 16;
+    if ((int64_t)M * g.x_row_bytes > 48 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
+    g.x_off = g.NS * g.S * g.stride;
+    g.bar_off = (g.x_off + M * g.x_row_bytes + 15) / 16 * 16;
+    g.smem = (size_t)g.bar_off + 16 * g.NS;
+    if (g.smem > 232448) return BQG_ERR_UNSUPPORTED_SHAPE;
+
+    int bpsm = 0;
+    {
+        auto key = std::make_tuple(device, wf, xf, M, 0, g.threads, 1, g.smem);
+        std::unique_lock<std::mutex> lk(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) {
+            bpsm = it->second;
+        } else {
+            lk.unlock();
+            GemvParams dummy{};
+            const cudaError_t e = lpr_runner(wf, xf)(dummy, M, dim3(1), g.threads, g.smem, 0, false, &bpsm);
+            if (e != cudaSuccess) return cuda_status(e);
+            lk.lock();
+            g_occ[key] = bpsm;
+        }
+    }
+    if (bpsm < 1) return BQG_ERR_UNSUPPORTED_SHAPE;
+    bpsm = std::min(bpsm, ctas_per_sm_cap());
+    const int64_t units = Nv / unit;
+    const int64_t want = ((int64_t)dev.sms * bpsm + g.splits - 1) / g.splits;
+    g.ctas = (int)std::max<int64_t>(1, std::min(units, want));
+    g.grid = dim3((unsigned)g.ctas, (unsigned)g.splits);
+    g.ws_bytes = (g.splits > 1) ? (size_t)g.splits * M * Nv * sizeof(float) : 0;
+    *pl = g;
+    return BQG_OK;
+}
+
+// The plan a GEMV call uses: lanes-per-row when it applies, else K-slice.
+int plan_any(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevInfo &dev, int device, GemvPlan *g)
+{
+    int st = plan_lpr(wf, xf, M, Nv, K, unit, dev, device, g);
+    if (st == BQG_OK) return st;
+    if (st != BQG_ERR_UNSUPPORTED_SHAPE) return st;
+    return plan_gemv(wf, xf, M, Nv, K, unit, dev, device, g);
+}
 
 // Common path of every GEMV entry point.
 int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void *ws, size_t ws_bytes,
@@ -207,7 +349,7 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     if (p.Nv == 0) return BQG_OK;
     const int unit = (final_epi == EPI_SWIGLU) ? 2 : 1;
     GemvPlan g;
-    st = plan_gemv(wf, xf, M, p.Nv, K, unit, dev, dv, &g);
+    st = plan_any(wf, xf, M, p.Nv, K, unit, dev, dv, &g);
     if (st) return st;
     if (g.ws_bytes > 0) {
         if (!ws || ws_bytes < g.ws_bytes) return BQG_ERR_WORKSPACE;
@@ -226,11 +368,16 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     p.part_off = g.part_off;
     p.bar_off = g.bar_off;
     p.ctas = g.ctas;
+    p.L = g.L;
+    p.wg = g.wg;
+    p.ng = g.ng;
+    p.x_off = g.x_off;
+    p.x_row_bytes = g.x_row_bytes;
     p.ws = (float *)ws;
     p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;
     const bool pdl = g_pdl.load() != 0;
-    p.prefetch_rows = pdl ? g.NS * g.S : 0;
-    cudaError_t e = runner(wf, xf)(p, M, g.C, g.grid, g.threads, g.smem, stream, pdl, nullptr);
+    cudaError_t e = g.lpr ? lpr_runner(wf, xf)(p, M, g.grid, g.threads, g.smem, stream, pdl, nullptr)
+                          : runner(wf, xf)(p, M, g.C, g.grid, g.threads, g.smem, stream, pdl, nullptr);
     if (e != cudaSuccess) return cuda_status(e);
     if (g.splits > 1) {
         e = launch_splitk_reduce(p, M, g.splits, final_epi, stream, pdl);
@@ -435,7 +582,7 @@ size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K)
     default: return 0;
     }
     GemvPlan g;
-    if (plan_gemv(wf, xf, M, Nv, K, unit, dev, dv, &g) != BQG_OK) return 0;
+    if (plan_any(wf, xf, M, Nv, K, unit, dev, dv, &g) != BQG_OK) return 0;
     return g.ws_bytes;
 }
 

@@ -31,7 +31,7 @@
 namespace bqg {
 
 enum WFmt { W_BF16 = 0, W_Q8_0 = 1, W_Q4_0 = 2 };
-enum XFmt { X_BF16 = 0, X_Q8_1 = 1 };
+enum XFmt { X_BF16 = 0, X_Q8_1 = 1, X_F32 = 2 };   // X_F32: bf16 input held as fp32 in registers
 enum Epi { EPI_STORE = 0, EPI_SWIGLU = 1, EPI_PARTIAL = 2 };
 
 // elements covered by one chunk (one 16-byte code load)
@@ -58,7 +58,6 @@ struct GemvParams {
     int RG;                 // row groups per CTA
     int64_t rows_per_cta;   // virtual rows per CTA (multiple of 2 for gate/up)
     int chunks_per_split;   // chunk range of one split (grid.y)
-    int prefetch_rows;      // rows of this CTA to warm in L2 before griddepcontrol.wait
     // shared-memory pipeline
     int nstages;            // NS stages in the ring
     int stage_rows;         // S rows per stage (RG * rows per group per stage)
@@ -67,6 +66,12 @@ struct GemvParams {
     int part_off;           // byte offset of the partial sums
     int bar_off;            // byte offset of the mbarriers (8-byte aligned)
     int ctas;               // CTAs along grid.x (rows are split evenly over them)
+    // lanes-per-row kernel
+    int L;                  // lanes that share one row (8, 16 or 32)
+    int wg;                 // warps per stage group
+    int ng;                 // stage groups
+    int x_off;              // byte offset of the staged activations
+    int x_row_bytes;        // staged bytes of one activation row
 };
 
 // Error word set when a bounded wait gives up (one per translation unit).
@@ -125,6 +130,10 @@ template <int WF> struct XSlice<WF, X_BF16> {
     static constexpr int WORDS = ChunkTraits<WF>::E / 2;
     uint32_t w[WORDS];
 };
+// bf16 activations converted once to fp32 (E values per chunk)
+template <int WF> struct XSlice<WF, X_F32> {
+    float f[ChunkTraits<WF>::E];
+};
 // q8_1 activations (q4_0 weights only): 32 codes, d, and the exact sum of codes
 template <> struct XSlice<W_Q4_0, X_Q8_1> {
     int32_t q[8];
@@ -135,7 +144,25 @@ template <> struct XSlice<W_Q4_0, X_Q8_1> {
 template <int WF, int XF>
 __device__ __forceinline__ void load_x(XSlice<WF, XF> &xs, const GemvParams &p, int m, int c, bool valid)
 {
-    if constexpr (XF == X_BF16) {
+    if constexpr (XF == X_F32) {
+        constexpr int E = ChunkTraits<WF>::E;
+        if (!valid) {
+#pragma unroll
+            for (int i = 0; i < E; i++) xs.f[i] = 0.f;
+            return;
+        }
+        const uint8_t *src = p.X + ((int64_t)m * p.K + chunk_elem0<WF>(c)) * 2;
+#pragma unroll
+        for (int i = 0; i < E / 8; i++) {
+            const uint4 v = ldg_v4(src + 16 * i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                xs.f[8 * i + 2 * k] = bf16_lo(w[k]);
+                xs.f[8 * i + 2 * k + 1] = bf16_hi(w[k]);
+            }
+        }
+    } else if constexpr (XF == X_BF16) {
         constexpr int WORDS = XSlice<WF, XF>::WORDS;
         if (!valid) {
 #pragma unroll
@@ -225,7 +252,46 @@ template <int WF, int XF>
 __device__ __forceinline__ float chunk_dot(const WChunk<WF> &w, const XSlice<WF, XF> &x)
 {
     const uint32_t cw[4] = {w.c.x, w.c.y, w.c.z, w.c.w};
-    if constexpr (WF == W_BF16) {
+    if constexpr (XF == X_F32 && WF == W_BF16) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            a0 = fmaf(bf16_lo(cw[i]), x.f[2 * i], a0);
+            a1 = fmaf(bf16_hi(cw[i]), x.f[2 * i + 1], a1);
+        }
+        return a0 + a1;
+    } else if constexpr (XF == X_F32 && WF == W_Q8_0) {
+        constexpr float OFF = 8388608.0f + 128.0f;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t u = cw[i] ^ 0x80808080u;
+            a0 = fmaf(byte_plus_2p23<0>(u) - OFF, x.f[4 * i], a0);
+            a1 = fmaf(byte_plus_2p23<1>(u) - OFF, x.f[4 * i + 1], a1);
+            a0 = fmaf(byte_plus_2p23<2>(u) - OFF, x.f[4 * i + 2], a0);
+            a1 = fmaf(byte_plus_2p23<3>(u) - OFF, x.f[4 * i + 3], a1);
+        }
+        return (a0 + a1) * half_bits_to_float(w.s);
+    } else if constexpr (XF == X_F32 && WF == W_Q4_0) {
+        // q4_0 codes against fp32 activations: low nibbles of word i are
+        // elements 4i..4i+3, high nibbles 16+4i..16+4i+3
+        constexpr float OFF = 8388608.0f + 8.0f;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t lo = cw[i] & 0x0f0f0f0fu;
+            const uint32_t hi = (cw[i] >> 4) & 0x0f0f0f0fu;
+            a0 = fmaf(byte_plus_2p23<0>(lo) - OFF, x.f[4 * i], a0);
+            a1 = fmaf(byte_plus_2p23<1>(lo) - OFF, x.f[4 * i + 1], a1);
+            a0 = fmaf(byte_plus_2p23<2>(lo) - OFF, x.f[4 * i + 2], a0);
+            a1 = fmaf(byte_plus_2p23<3>(lo) - OFF, x.f[4 * i + 3], a1);
+            a0 = fmaf(byte_plus_2p23<0>(hi) - OFF, x.f[16 + 4 * i], a0);
+            a1 = fmaf(byte_plus_2p23<1>(hi) - OFF, x.f[16 + 4 * i + 1], a1);
+            a0 = fmaf(byte_plus_2p23<2>(hi) - OFF, x.f[16 + 4 * i + 2], a0);
+            a1 = fmaf(byte_plus_2p23<3>(hi) - OFF, x.f[16 + 4 * i + 3], a1);
+        }
+        return (a0 + a1) * half_bits_to_float(w.s);
+    } else if constexpr (WF == W_BF16) {
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; i++) {
@@ -276,7 +342,7 @@ __device__ __forceinline__ void named_barrier(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// rows each group takes from a stage; V = RPS * M values per warp reduction
+// rows each group takes from a stage (per pass); V = RPS * M values per warp reduction
 template <int M> struct RowsPerStage { static constexpr int value = (M == 8) ? 1 : 4 / M; };
 
 // This CTA's virtual rows [v0, v1): an even split of Nv over p.ctas CTAs
@@ -289,14 +355,84 @@ __device__ __forceinline__ void cta_rows(const GemvParams &p, int64_t &v0, int64
     v1 = (int64_t)(blockIdx.x + 1) * units / p.ctas * unit;
 }
 
+// Virtual row held by staged row r of a stage that starts at virtual row vs.
+// With gate/up pairs a stage of S rows holds S/2 gate rows then the S/2 up
+// rows of the same outputs, so each half is one contiguous run in memory.
+__device__ __forceinline__ int64_t staged_vrow(const GemvParams &p, int64_t vs, int S, int r)
+{
+    if (p.nmat == 2) {
+        const int half = S >> 1;
+        return (r < half) ? vs + 2 * r : vs + 2 * (r - half) + 1;
+    }
+    return vs + r;
+}
+
+// The producer lane: streams stages [0, nst) of this CTA's rows into the
+// ring with cp.async.bulk, one copy per run of consecutive rows of one
+// matrix.  The first NS stages are requested before waiting for the
+// previous grid on the stream: weights do not depend on it (the documented
+// contract of programmatic dependent launch), so this call's weight stream
+// overlaps the previous kernel's tail.
+template <int WF>
+__device__ __forceinline__ void produce_stages(const GemvParams &p, uint8_t *smem, uint32_t bar0, int64_t v0,
+                                               int64_t v1, int64_t roff, int64_t rbytes, int nst, int *s_abort)
+{
+    const int S = p.stage_rows;
+    const int NS = p.nstages;
+    const int stage_bytes = S * p.row_stride;
+    const bool whole_rows = (roff == 0 && rbytes == p.row_bytes);
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    for (int j = 0; j < nst; j++) {
+        if (j == NS) { pdl_wait(); pdl_launch_dependents(); }
+        if (j >= NS && !mbar_wait_bounded(bar0 + 8 * (NS + s), ph ^ 1)) {
+            atomicExch(&g_gemv_error, 1);
+            *s_abort = 1;
+            break;
+        }
+        if (*(volatile int *)s_abort) break;
+        const int64_t vs = v0 + (int64_t)j * S;
+        const uint32_t dst = smem_u32(smem) + (uint32_t)(s * stage_bytes);
+        int nvalid = 0;
+        for (int r = 0; r < S; r++) nvalid += staged_vrow(p, vs, S, r) < v1;
+        mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(nvalid * rbytes));
+        for (int r = 0; r < S;) {
+            const int64_t v = staged_vrow(p, vs, S, r);
+            if (v >= v1) { r++; continue; }
+            int mat; int64_t rr;
+            map_row(p, v, mat, rr);
+            int len = 1;
+            while (whole_rows && r + len < S) {
+                const int64_t vn = staged_vrow(p, vs, S, r + len);
+                if (vn >= v1) break;
+                int mn; int64_t rn;
+                map_row(p, vn, mn, rn);
+                if (mn != mat || rn != rr + len) break;
+                len++;
+            }
+            bulk_g2s(dst + r * p.row_stride, p.W[mat] + rr * p.row_bytes + roff, (uint32_t)(len * rbytes),
+                     bar0 + 8 * s);
+            r += len;
+        }
+        issued = j + 1;
+        if (++s == NS) { s = 0; ph ^= 1; }
+    }
+    if (nst <= NS) { pdl_wait(); pdl_launch_dependents(); }
+    // do not leave while copies into this CTA's shared memory are in flight
+    for (int j = max(0, issued - NS); j < issued; j++)
+        mbar_wait_bounded(bar0 + 8 * (j % NS), (uint32_t)((j / NS) & 1));
+}
+
 // ---------------------------------------------------------------------------
 // the kernel: one producer warp streams the CTA's rows into a ring of
-// shared-memory stages with cp.async.bulk; RG x TPR consumer threads read
-// their K-slice of each staged row against activations held in registers.
-// Per-row partial sums of each warp go to shared memory and are combined
-// (in warp order, so results are deterministic) once per window of rows.
-// Every wait on an mbarrier is bounded; on a timeout the kernel records an
-// error in g_gemv_error and finishes without reading stale data.
+// shared-memory stages with cp.async.bulk (one copy per contiguous run of
+// rows); RG x TPR consumer threads read their K-slice of each staged row
+// against activations held in registers.  Per-row partial sums of each warp
+// go to shared memory and are combined (in warp order, so results are
+// deterministic) once per window of rows.  Every wait on an mbarrier is
+// bounded; on a timeout the kernel records an error in g_gemv_error and
+// finishes without reading stale data.
 // ---------------------------------------------------------------------------
 template <int WF, int XF, int M, int C>
 __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvParams p)
@@ -310,8 +446,9 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int ncons = p.RG * p.TPR;                // consumer threads (a multiple of 32)
-    const int S = p.stage_rows;
+    const int S = p.stage_rows;                    // SUB * RG * RPS
     const int NS = p.nstages;
+    const int stage_bytes = S * p.row_stride;
     uint8_t *stages = smem;
     float *part = reinterpret_cast<float *>(smem + p.part_off);
     const uint32_t bar0 = smem_u32(smem + p.bar_off);   // full[NS] then empty[NS]
@@ -323,7 +460,8 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
     const int cend = min(p.nc, cbeg + p.chunks_per_split);
     int64_t roff, rbytes;
     chunk_range_bytes<WF>(cbeg, cend, roff, rbytes);
-    const int64_t nst = (v1 - v0 + S - 1) / S;      // stages this CTA streams
+    const int nrows = (int)(v1 - v0);
+    const int nst = (nrows + S - 1) / S;            // stages this CTA streams
 
     if (tid == 0) {
         for (int i = 0; i < NS; i++) {
@@ -336,41 +474,7 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
     __syncthreads();
 
     if (tid >= ncons) {
-        // ---------------- producer warp ----------------
-        if (lane != 0) return;
-        if (p.prefetch_rows > 0) {          // warm L2 before the previous grid ends
-            const int64_t npf = min((int64_t)p.prefetch_rows, v1 - v0);
-            for (int64_t j = 0; j < npf; j++) {
-                int mat; int64_t rr;
-                map_row(p, v0 + j, mat, rr);
-                prefetch_l2_bulk(p.W[mat] + rr * p.row_bytes + roff, (uint32_t)rbytes);
-            }
-        }
-        pdl_wait();
-        pdl_launch_dependents();
-        int64_t issued = 0;
-        for (int64_t j = 0; j < nst; j++) {
-            const int s = (int)(j % NS);
-            if (j >= NS && !mbar_wait_bounded(bar0 + 8 * (NS + s), (uint32_t)(((j / NS) - 1) & 1))) {
-                atomicExch(&g_gemv_error, 1);
-                s_abort = 1;
-                break;
-            }
-            if (*(volatile int *)&s_abort) break;
-            const int64_t vs = v0 + j * S;
-            const int nrow = (int)min((int64_t)S, v1 - vs);
-            mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(nrow * rbytes));
-            const uint32_t dst = smem_u32(stages) + (uint32_t)s * (uint32_t)(S * p.row_stride);
-            for (int r = 0; r < nrow; r++) {
-                int mat; int64_t rr;
-                map_row(p, vs + r, mat, rr);
-                bulk_g2s(dst + r * p.row_stride, p.W[mat] + rr * p.row_bytes + roff, (uint32_t)rbytes, bar0 + 8 * s);
-            }
-            issued = j + 1;
-        }
-        // do not leave while copies into this CTA's shared memory are in flight
-        for (int64_t j = max((int64_t)0, issued - NS); j < issued; j++)
-            mbar_wait_bounded(bar0 + 8 * (int)(j % NS), (uint32_t)((j / NS) & 1));
+        if (lane == 0) produce_stages<WF>(p, smem, bar0, v0, v1, roff, rbytes, nst, &s_abort);
         return;
     }
 
@@ -381,71 +485,84 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
     const int tau = tid - g * p.TPR;       // thread in group
     const int wig = tau >> 5;              // warp in group
     const int WPG = p.TPR >> 5;
+    const int SUB = S / (p.RG * RPS);      // passes over a stage
 
-    int cid[C];
+    int coff[C], soff[C];
     bool cval[C];
-#pragma unroll
-    for (int i = 0; i < C; i++) {
-        cid[i] = cbeg + tau + i * p.TPR;
-        cval[i] = cid[i] < cend && chunk_valid<WF>(cid[i], p.nb, p.nc);
-    }
     XSlice<WF, XF> xs[C][M];
 #pragma unroll
-    for (int i = 0; i < C; i++)
+    for (int i = 0; i < C; i++) {
+        const int c = cbeg + tau + i * p.TPR;
+        cval[i] = c < cend && chunk_valid<WF>(c, p.nb, p.nc);
+        coff[i] = (int)(chunk_code_off<WF>(c) - roff);
+        soff[i] = (WF == W_BF16) ? 0 : (int)(chunk_scale_off<WF>(c) - roff);
 #pragma unroll
-        for (int m = 0; m < M; m++) load_x<WF, XF>(xs[i][m], p, m, cid[i], cval[i]);
+        for (int m = 0; m < M; m++) load_x<WF, XF>(xs[i][m], p, m, c, cval[i]);
+    }
 
     const int64_t WIN = (int64_t)p.win_stages * S;
     int64_t win0 = v0;
+    int s = 0, wstage = 0;
+    uint32_t ph = 0;
     bool ok = true;
-    for (int64_t j = 0; j < nst; j++) {
-        const int s = (int)(j % NS);
-        if (ok && !mbar_wait_bounded(bar0 + 8 * s, (uint32_t)((j / NS) & 1))) {
+    for (int j = 0; j < nst; j++) {
+        if (ok && !mbar_wait_bounded(bar0 + 8 * s, ph)) {
             atomicExch(&g_gemv_error, 1);
             s_abort = 1;
         }
         ok = ok && !*(volatile int *)&s_abort;
-        const int64_t vs = v0 + j * S;
-        const uint8_t *stage = stages + (size_t)s * S * p.row_stride;
-        float acc[V];
+        const int64_t vs = v0 + (int64_t)j * S;
+        const bool full = ok && (vs + S <= v1);
+        const uint8_t *stage = stages + s * stage_bytes;
+        for (int sub = 0; sub < SUB; sub++) {
+            float acc[V];
 #pragma unroll
-        for (int rr = 0; rr < RPS; rr++) {
-            const int r = g + p.RG * rr;
-            const bool rv = ok && (vs + r < v1);
-            const uint8_t *srow = stage + (size_t)r * p.row_stride;
-            WChunk<WF> wc[C];
+            for (int rr = 0; rr < RPS; rr++) {
+                const int r = (sub * RPS + rr) * p.RG + g;
+                const bool rv = full || (ok && staged_vrow(p, vs, S, r) < v1);
+                const uint8_t *srow = stage + r * p.row_stride;
+                WChunk<WF> wc[C];
 #pragma unroll
-            for (int i = 0; i < C; i++) {
-                if (rv && cval[i]) lds_w<WF>(wc[i], srow, roff, cid[i]);
-                else { wc[i].c = make_uint4(0, 0, 0, 0); wc[i].s = 0; }
+                for (int i = 0; i < C; i++) {
+                    if (rv && cval[i]) {
+                        wc[i].c = *reinterpret_cast<const uint4 *>(srow + coff[i]);
+                        wc[i].s = (WF == W_BF16) ? 0u : (uint32_t)*reinterpret_cast<const uint16_t *>(srow + soff[i]);
+                    } else {
+                        wc[i].c = make_uint4(0, 0, 0, 0);
+                        wc[i].s = 0;
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < M; m++) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int i = 0; i < C; i++) a += chunk_dot<WF, XF>(wc[i], xs[i][m]);
+                    acc[rr * M + m] = a;
+                }
             }
-#pragma unroll
-            for (int m = 0; m < M; m++) {
-                float a = 0.f;
-#pragma unroll
-                for (int i = 0; i < C; i++) a += chunk_dot<WF, XF>(wc[i], xs[i][m]);
-                acc[rr * M + m] = a;
+            if (sub == SUB - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar0 + 8 * (NS + s));   // this warp is done with stage s
+            }
+            const float tot = WR::run(acc, lane);
+            if (WR::is_holder(lane)) {
+                const int idx = WR::index_of_lane(lane);
+                const int rr = idx / M, m = idx - (idx / M) * M;
+                const int64_t v = staged_vrow(p, vs, S, (sub * RPS + rr) * p.RG + g);
+                if (v < v1) part[((int)(v - win0) * WPG + wig) * M + m] = tot;
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar0 + 8 * (NS + s));     // this warp is done with stage s
-
-        const float tot = WR::run(acc, lane);
-        if (WR::is_holder(lane)) {
-            const int idx = WR::index_of_lane(lane);
-            const int rr = idx / M, m = idx - (idx / M) * M;
-            const int64_t v = vs + g + (int64_t)p.RG * rr;
-            if (v < v1) part[((v - win0) * WPG + wig) * M + m] = tot;
-        }
+        if (++s == NS) { s = 0; ph ^= 1; }
 
         // window complete: combine the warps' partials (warp order) and store
-        if ((j + 1) % p.win_stages == 0 || j + 1 == nst) {
+        if (++wstage == p.win_stages || j + 1 == nst) {
+            wstage = 0;
             named_barrier(1, ncons);
-            const int64_t nrw = min(WIN, v1 - win0);
+            const int nrw = (int)min(WIN, v1 - win0);
             if (p.epi == EPI_SWIGLU) {
-                for (int64_t t = tid; t < (nrw >> 1) * M; t += ncons) {
-                    const int64_t pr = t / M;
-                    const int m = (int)(t - pr * M);
+                for (int t = tid; t < (nrw >> 1) * M; t += ncons) {
+                    const int pr = t / M;
+                    const int m = t - pr * M;
                     float gs = 0.f, us = 0.f;
                     for (int w = 0; w < WPG; w++) {
                         gs += part[((2 * pr) * WPG + w) * M + m];
@@ -454,9 +571,9 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
                     p.Y[0][(int64_t)m * p.rows[0] + ((win0 >> 1) + pr)] = silu(gs) * us;
                 }
             } else {
-                for (int64_t t = tid; t < nrw * M; t += ncons) {
-                    const int64_t row = t / M;
-                    const int m = (int)(t - row * M);
+                for (int t = tid; t < nrw * M; t += ncons) {
+                    const int row = t / M;
+                    const int m = t - row * M;
                     float sum = 0.f;
                     for (int w = 0; w < WPG; w++) sum += part[(row * WPG + w) * M + m];
                     const int64_t v = win0 + row;
@@ -473,6 +590,253 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
             win0 += WIN;
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Staged activations for the lanes-per-row kernel.  Chunk c of activation
+// row m is P pieces of 16 bytes; piece p of chunks 32u .. 32u+31 is one run
+// of 512 bytes, so lanes reading consecutive chunks hit distinct banks.
+// q8_1 rows add, per block, (d as float, exact sum of codes) after the runs.
+// ---------------------------------------------------------------------------
+template <int WF, int XF> struct XPieces { static constexpr int P = ChunkTraits<WF>::E / 4; };   // fp32
+template <> struct XPieces<W_Q4_0, X_Q8_1> { static constexpr int P = 2; };                    // 32 codes
+
+template <int WF, int XF>
+__host__ __device__ __forceinline__ int x_stage_row_bytes(int nc, int nb)
+{
+    const int runs = (nc + 31) / 32;
+    return runs * XPieces<WF, XF>::P * 512 + ((XF == X_Q8_1) ? nb * 8 : 0);
+}
+
+template <int WF, int XF>
+__device__ __forceinline__ void stage_x(const GemvParams &p, uint8_t *xs, int M, int tid, int nthr)
+{
+    constexpr int P = XPieces<WF, XF>::P;
+    const int runs = (p.nc + 31) / 32;
+    for (int m = 0; m < M; m++) {
+        uint8_t *xr = xs + (size_t)m * p.x_row_bytes;
+        for (int i = tid; i < p.nc * P; i += nthr) {
+            const int c = i / P, pc = i - (i / P) * P;
+            if (!chunk_valid<WF>(c, p.nb, p.nc)) continue;
+            uint4 v;
+            if constexpr (XF == X_Q8_1) {
+                const uint32_t *blk = reinterpret_cast<const uint32_t *>(p.X + ((int64_t)m * p.nb + c) * Q8_1_BYTES);
+                v = make_uint4(__ldg(blk + 1 + 4 * pc), __ldg(blk + 2 + 4 * pc), __ldg(blk + 3 + 4 * pc),
+                               __ldg(blk + 4 + 4 * pc));
+                if (pc == 0) {
+                    int sum = 0;
+                    for (int k = 0; k < 8; k++) sum = __dp4a((int)__ldg(blk + 1 + k), 0x01010101, sum);
+                    float2 ds = make_float2(half_bits_to_float(__ldg(blk) & 0xffffu), __int_as_float(sum));
+                    *reinterpret_cast<float2 *>(xr + (size_t)runs * P * 512 + (size_t)c * 8) = ds;
+                }
+            } else {
+                // four consecutive bf16 -> fp32
+                const uint2 w = __ldg(reinterpret_cast<const uint2 *>(
+                    p.X + ((int64_t)m * p.K + chunk_elem0<WF>(c) + 4 * pc) * 2));
+                v = make_uint4(w.x << 16, w.x & 0xffff0000u, w.y << 16, w.y & 0xffff0000u);
+            }
+            *reinterpret_cast<uint4 *>(xr + ((size_t)(c >> 5) * P + pc) * 512 + (c & 31) * 16) = v;
+        }
+    }
+}
+
+template <int WF, int XF>
+__device__ __forceinline__ void lds_x(XSlice<WF, XF> &x, const uint8_t *xr, int c, int runs)
+{
+    constexpr int P = XPieces<WF, XF>::P;
+    const uint8_t *base = xr + (size_t)(c >> 5) * P * 512 + (c & 31) * 16;
+    if constexpr (XF == X_Q8_1) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(base);
+        const uint4 b = *reinterpret_cast<const uint4 *>(base + 512);
+        x.q[0] = a.x; x.q[1] = a.y; x.q[2] = a.z; x.q[3] = a.w;
+        x.q[4] = b.x; x.q[5] = b.y; x.q[6] = b.z; x.q[7] = b.w;
+        const float2 ds = *reinterpret_cast<const float2 *>(xr + (size_t)runs * P * 512 + (size_t)c * 8);
+        x.d = ds.x;
+        x.sum = __float_as_int(ds.y);
+    } else {
+#pragma unroll
+        for (int pc = 0; pc < P; pc++) {
+            const float4 f = *reinterpret_cast<const float4 *>(base + pc * 512);
+            x.f[4 * pc] = f.x; x.f[4 * pc + 1] = f.y; x.f[4 * pc + 2] = f.z; x.f[4 * pc + 3] = f.w;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Lanes-per-row kernel (M = 1, 2).  The producer warp streams small stages
+// of rows into the same shared-memory ring as gemv_kernel.  Consumer warps
+// form NG groups of WG warps; group g takes stages g, g + NG, ... so many
+// warps work while each stage stays small.  Within a stage every warp takes
+// R = 32/L rows; the L lanes of a row walk its K range (chunks sub,
+// sub + L, ...) in a tight loop, reading weights from the staged row and
+// activations from a shared-memory copy made once per CTA, and accumulate
+// one register per output.  One L-lane shuffle reduction finishes each row,
+// which is stored at once: no cross-warp partials and no barriers in the
+// loop.
+// ---------------------------------------------------------------------------
+template <int WF, int XF, int M>
+__global__ void __launch_bounds__(544, 1) gemv_lpr_kernel(const GemvParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int ncons = p.TPR;                       // consumer threads = 32 * NG * WG
+    const int S = p.stage_rows;                    // WG * R rows per stage
+    const int NS = p.nstages;
+    const int stage_bytes = S * p.row_stride;
+    uint8_t *xs = smem + p.x_off;
+    const uint32_t bar0 = smem_u32(smem + p.bar_off);
+
+    int64_t v0, v1;
+    cta_rows(p, v0, v1);
+    const int split = blockIdx.y;
+    const int cbeg = split * p.chunks_per_split;
+    const int cend = min(p.nc, cbeg + p.chunks_per_split);
+    int64_t roff, rbytes;
+    chunk_range_bytes<WF>(cbeg, cend, roff, rbytes);
+    const int nrows = (int)(v1 - v0);
+    const int nst = (nrows + S - 1) / S;
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; i++) {
+            mbar_init(bar0 + 8 * i, 1);                 // full: producer's arrive + bytes
+            mbar_init(bar0 + 8 * (NS + i), p.wg);       // empty: the group's warps
+        }
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (tid >= ncons) {
+        if (lane == 0) produce_stages<WF>(p, smem, bar0, v0, v1, roff, rbytes, nst, &s_abort);
+        return;
+    }
+
+    pdl_wait();
+    pdl_launch_dependents();
+    stage_x<WF, XF>(p, xs, M, tid, ncons);
+    named_barrier(1, ncons);
+
+    const int L = p.L;
+    const int lgL = 31 - __clz(L);
+    const int R = 32 >> lgL;                       // rows per warp per stage
+    const int q = lane >> lgL;                     // which of the warp's rows
+    const int sub = lane & (L - 1);                // lane within the row
+    const int runs = (p.nc + 31) / 32;
+    const bool swiglu = (p.epi == EPI_SWIGLU);
+    const int grp = warp / p.wg;
+    const int wig = warp - grp * p.wg;
+    const int pr = wig * R + q;                    // row slot within a stage
+    const int r = swiglu ? ((pr >> 1) + ((pr & 1) ? (S >> 1) : 0)) : pr;
+    const int c0 = cbeg + sub;
+    const int J = (c0 < cend) ? (cend - c0 + L - 1) >> lgL : 0;
+    const uint8_t *xm = xs;
+
+    int s = grp % NS;
+    uint32_t ph = (uint32_t)((grp / NS) & 1);
+    bool ok = true;
+    for (int j = grp; j < nst; j += p.ng) {
+        if (ok && !mbar_wait_bounded(bar0 + 8 * s, ph)) {
+            atomicExch(&g_gemv_error, 1);
+            s_abort = 1;
+        }
+        ok = ok && !*(volatile int *)&s_abort;
+        const int64_t vs = v0 + (int64_t)j * S;
+        const int64_t v = staged_vrow(p, vs, S, r);
+        const bool rv = ok && v < v1;
+        const uint8_t *srow = smem + s * stage_bytes + r * p.row_stride;
+
+        float acc[M];
+#pragma unroll
+        for (int m = 0; m < M; m++) acc[m] = 0.f;
+        if (rv) {
+#pragma unroll 4
+            for (int jj = 0; jj < J; jj++) {
+                const int c = c0 + (jj << lgL);
+                if (WF == W_Q8_0 && !chunk_valid<WF>(c, p.nb, p.nc)) continue;
+                WChunk<WF> wc;
+                lds_w<WF>(wc, srow, roff, c);
+#pragma unroll
+                for (int m = 0; m < M; m++) {
+                    XSlice<WF, XF> x;
+                    lds_x<WF, XF>(x, xm + m * p.x_row_bytes, c, runs);
+                    acc[m] += chunk_dot<WF, XF>(wc, x);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar0 + 8 * (NS + s));       // this warp is done with stage s
+        s += p.ng;
+        while (s >= NS) { s -= NS; ph ^= 1; }
+
+        // finish the row over its L lanes (fixed butterfly order)
+#pragma unroll
+        for (int m = 0; m < M; m++)
+            for (int off = L >> 1; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
+        if (swiglu) {
+            // lane groups 2i (gate) and 2i+1 (up) hold one output
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                const float u = __shfl_down_sync(0xffffffffu, acc[m], L);
+                if (rv && sub == 0 && (q & 1) == 0)
+                    p.Y[0][(int64_t)m * p.rows[0] + (v >> 1)] = silu(acc[m]) * u;
+            }
+        } else if (rv && sub == 0) {
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                if (p.epi == EPI_PARTIAL) {
+                    p.ws[((int64_t)split * M + m) * p.Nv + v] = acc[m];
+                } else {
+                    int mat; int64_t rr;
+                    map_row(p, v, mat, rr);
+                    p.Y[mat][(int64_t)m * p.rows[mat] + rr] = acc[m];
+                }
+            }
+        }
+    }
+}
+
+template <int WF, int XF, int M>
+__host__ cudaError_t gemv_lpr_launch_one(const GemvParams &p, dim3 grid, int threads, size_t smem,
+                                         cudaStream_t stream, bool pdl, int *occupancy)
+{
+    auto kern = gemv_lpr_kernel<WF, XF, M>;
+    if (occupancy) {
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+        if (e == cudaSuccess && smem + fa.sharedSizeBytes > (size_t)optin) return cudaErrorInvalidValue;
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, threads, smem);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int WF, int XF>
+__host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, int threads, size_t smem,
+                                       cudaStream_t stream, bool pdl, int *occupancy)
+{
+    constexpr int XR = (XF == X_BF16) ? X_F32 : XF;      // staged bf16 activations are fp32
+    if (M == 1) return gemv_lpr_launch_one<WF, XR, 1>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 2) return gemv_lpr_launch_one<WF, XR, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+    return cudaErrorInvalidValue;
 }
 
 // Split-K finish: Y = sum over splits (in split order) of the partials,
@@ -547,13 +911,20 @@ __host__ inline cudaError_t gemv_take_error(int *out)
     return v ? cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(int)) : cudaSuccess;
 }
 
+// bf16 activations are held as fp32 in registers where that costs few
+// registers (it saves one conversion per element per output row).
+template <int WF, int XF, int M> struct ActRep {
+    static constexpr int value =
+        (XF == X_BF16 && ((WF == W_BF16 && M <= 4) || (WF == W_Q8_0 && M <= 2))) ? X_F32 : XF;
+};
+
 template <int WF, int XF>
 __host__ cudaError_t gemv_dispatch(const GemvParams &p, int M, int C, dim3 grid, int threads, size_t smem,
                                    cudaStream_t stream, bool pdl, int *occupancy)
 {
 #define BQG_CASE(MM, CC)                                                                 \
     if (M == MM && C == CC)                                                              \
-        return gemv_launch_one<WF, XF, MM, CC>(p, grid, threads, smem, stream, pdl, occupancy);
+        return gemv_launch_one<WF, ActRep<WF, XF, MM>::value, MM, CC>(p, grid, threads, smem, stream, pdl, occupancy);
     BQG_CASE(1, 1) BQG_CASE(1, 2) BQG_CASE(1, 4)
     BQG_CASE(2, 1) BQG_CASE(2, 2) BQG_CASE(2, 4)
     BQG_CASE(4, 1) BQG_CASE(4, 2) BQG_CASE(4, 4)
