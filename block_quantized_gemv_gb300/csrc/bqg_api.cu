@@ -19,10 +19,10 @@ cudaError_t gemv_error_bf16(int *);
 cudaError_t gemv_error_q8_0(int *);
 cudaError_t gemv_error_q4_0(int *);
 cudaError_t gemv_error_q4_0_q8_1(int *);
-cudaError_t gemv_lpr_run_bf16(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
-cudaError_t gemv_lpr_run_q8_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
-cudaError_t gemv_lpr_run_q4_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
-cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_bf16(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q8_0(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q4_0(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
 int gemv_x_stage_bytes_bf16(int, int);
 int gemv_x_stage_bytes_q8_0(int, int);
 int gemv_x_stage_bytes_q4_0(int, int);
@@ -114,7 +114,7 @@ RunFn runner(int wf, int xf)
     return gemv_run_q4_0;
 }
 
-using LprFn = cudaError_t (*)(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+using LprFn = cudaError_t (*)(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
 LprFn lpr_runner(int wf, int xf)
 {
     if (xf == X_Q8_1) return gemv_lpr_run_q4_0_q8_1;
@@ -132,6 +132,7 @@ int x_stage_bytes(int wf, int xf, int nc, int nb)
 
 struct GemvPlan {
     bool lpr;               // lanes-per-row kernel (M <= 2)
+    bool compact;           // its compact configuration (small weight share per SM)
     int L, x_off, x_row_bytes, wg, ng;
     int C, TPR, RG, RPS, nc, cps, splits, threads, ncons, S, NS, stride, win_stages, part_off, bar_off, ctas;
     dim3 grid;
@@ -147,6 +148,9 @@ constexpr int kStageBudget = 100 * 1024;
 // Tuning knobs read once from the environment (unset = defaults above):
 //   BQG_STAGE_KB     staged-weight budget per CTA in KiB
 //   BQG_CTAS_PER_SM  cap on resident GEMV CTAs per SM (1 or 2)
+//   BQG_COMPACT_KB   run the compact lanes-per-row configuration when each
+//                    SM's weight share is at most this many KiB (default 0)
+//   BQG_NO_LPR       1: serve M <= 2 with the K-slice kernel
 int env_int(const char *name, int dflt)
 {
     const char *v = getenv(name);
@@ -276,6 +280,13 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
         if (g.splits >= maxs) return BQG_ERR_UNSUPPORTED_SHAPE;
         g.splits++;
     }
+    // A small weight share per SM runs the compact configuration, which lets
+    // the next call's CTAs share the SM and start streaming early.
+    const int64_t per_sm = Nv * (int64_t)g.stride * g.splits / std::max(1, dev.sms);
+    static const int compact_kb = env_int("BQG_COMPACT_KB", 0);   // off unless asked for
+    g.compact = per_sm <= (int64_t)compact_kb * 1024;
+    const int budget = g.compact ? 44 * 1024 : stage_budget();
+    const int max_warps = g.compact ? 8 : 16;
     // lanes per row: at least eight chunks per lane; gate/up pairs need two rows per warp
     g.L = (g.cps >= 256) ? 32 : (g.cps >= 128) ? 16 : 8;
     if (unit == 2 && g.L == 32) g.L = 16;
@@ -285,8 +296,9 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     rows = std::max(R, rows / R * R);
     g.S = rows;
     const int wg = g.S / R;
-    g.NS = (int)std::max<int64_t>(2, std::min<int64_t>(16, stage_budget() / ((int64_t)g.S * g.stride)));
-    const int ng = std::max(1, std::min(g.NS, 16 / wg));
+    g.NS = (int)std::max<int64_t>(2, std::min<int64_t>(16, budget / ((int64_t)g.S * g.stride)));
+    const int ng = std::max(1, std::min(g.NS, max_warps / wg));
+    if (wg > max_warps) return BQG_ERR_UNSUPPORTED_SHAPE;
     g.wg = wg;
     g.ng = ng;
     g.TPR = 32 * wg * ng;
@@ -303,7 +315,7 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
 
     int bpsm = 0;
     {
-        auto key = std::make_tuple(device, wf, xf, M, 0, g.threads, 1, g.smem);
+        auto key = std::make_tuple(device, wf, xf, M, g.compact ? 1 : 0, g.threads, 1, g.smem);
         std::unique_lock<std::mutex> lk(g_mu);
         auto it = g_occ.find(key);
         if (it != g_occ.end()) {
@@ -311,7 +323,7 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
         } else {
             lk.unlock();
             GemvParams dummy{};
-            const cudaError_t e = lpr_runner(wf, xf)(dummy, M, dim3(1), g.threads, g.smem, 0, false, &bpsm);
+            const cudaError_t e = lpr_runner(wf, xf)(dummy, M, g.compact, dim3(1), g.threads, g.smem, 0, false, &bpsm);
             if (e != cudaSuccess) return cuda_status(e);
             lk.lock();
             g_occ[key] = bpsm;
@@ -376,7 +388,7 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     p.ws = (float *)ws;
     p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;
     const bool pdl = g_pdl.load() != 0;
-    cudaError_t e = g.lpr ? lpr_runner(wf, xf)(p, M, g.grid, g.threads, g.smem, stream, pdl, nullptr)
+    cudaError_t e = g.lpr ? lpr_runner(wf, xf)(p, M, g.compact, g.grid, g.threads, g.smem, stream, pdl, nullptr)
                           : runner(wf, xf)(p, M, g.C, g.grid, g.threads, g.smem, stream, pdl, nullptr);
     if (e != cudaSuccess) return cuda_status(e);
     if (g.splits > 1) {

@@ -92,13 +92,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
 }
 // ~1 s at 2 GHz: no correct launch waits this long on one phase.
 constexpr long long kWaitTimeoutCycles = 1ll << 31;
-// Wait for the phase with the given parity; false if it did not complete in time.
+// Wait for the phase with the given parity; false if it did not complete in
+// time.  Between failed tests the warp sleeps (backing off to ~0.5 us) so
+// that waiting warps leave the issue slots to the warps doing work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
+    unsigned ns = 32;
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(ns);
+        ns = min(ns * 2, 512u);
         if (clock64() - t0 > kWaitTimeoutCycles) return false;
+    }
     return true;
 }
 // Bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.
@@ -127,6 +133,33 @@ template <int J>
 __device__ __forceinline__ float byte_plus_2p23(uint32_t w)
 {
     return __uint_as_float(__byte_perm(w, 0x4b000000u, J | (4 << 4) | (4 << 8) | (7 << 12)));
+}
+
+// ---------------------------------------------------------------------------
+// packed fp32 pairs (sm_100+): one instruction for two lanes of work
+// ---------------------------------------------------------------------------
+// (d0, d1) += (a0, a1) * (b0, b1), each with one rounding
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rd, {%0, %1};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (a0 + c, a1 + c) with one rounding each
+__device__ __forceinline__ void fadd2(float &a0, float &a1, float c)
+{
+    asm("{\n\t.reg .b64 ra, rc;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rc, {%2, %2};\n\t"
+        "add.rn.f32x2 ra, ra, rc;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(c));
 }
 
 // ---------------------------------------------------------------------------

@@ -255,42 +255,47 @@ __device__ __forceinline__ float chunk_dot(const WChunk<WF> &w, const XSlice<WF,
     if constexpr (XF == X_F32 && WF == W_BF16) {
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            a0 = fmaf(bf16_lo(cw[i]), x.f[2 * i], a0);
-            a1 = fmaf(bf16_hi(cw[i]), x.f[2 * i + 1], a1);
-        }
+        for (int i = 0; i < 4; i++) ffma2(a0, a1, bf16_lo(cw[i]), bf16_hi(cw[i]), x.f[2 * i], x.f[2 * i + 1]);
         return a0 + a1;
     } else if constexpr (XF == X_F32 && WF == W_Q8_0) {
+        // codes are int8 q; byte ^ 0x80 = q + 128; pairs of elements go through
+        // one packed subtract and one packed FMA
         constexpr float OFF = 8388608.0f + 128.0f;
-        float a0 = 0.f, a1 = 0.f;
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const uint32_t u = cw[i] ^ 0x80808080u;
-            a0 = fmaf(byte_plus_2p23<0>(u) - OFF, x.f[4 * i], a0);
-            a1 = fmaf(byte_plus_2p23<1>(u) - OFF, x.f[4 * i + 1], a1);
-            a0 = fmaf(byte_plus_2p23<2>(u) - OFF, x.f[4 * i + 2], a0);
-            a1 = fmaf(byte_plus_2p23<3>(u) - OFF, x.f[4 * i + 3], a1);
+            float e0 = byte_plus_2p23<0>(u), e1 = byte_plus_2p23<1>(u);
+            float e2 = byte_plus_2p23<2>(u), e3 = byte_plus_2p23<3>(u);
+            fadd2(e0, e1, -OFF);
+            fadd2(e2, e3, -OFF);
+            ffma2(a0, a1, e0, e1, x.f[4 * i], x.f[4 * i + 1]);
+            ffma2(b0, b1, e2, e3, x.f[4 * i + 2], x.f[4 * i + 3]);
         }
-        return (a0 + a1) * half_bits_to_float(w.s);
+        return ((a0 + a1) + (b0 + b1)) * half_bits_to_float(w.s);
     } else if constexpr (XF == X_F32 && WF == W_Q4_0) {
         // q4_0 codes against fp32 activations: low nibbles of word i are
         // elements 4i..4i+3, high nibbles 16+4i..16+4i+3
         constexpr float OFF = 8388608.0f + 8.0f;
-        float a0 = 0.f, a1 = 0.f;
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const uint32_t lo = cw[i] & 0x0f0f0f0fu;
             const uint32_t hi = (cw[i] >> 4) & 0x0f0f0f0fu;
-            a0 = fmaf(byte_plus_2p23<0>(lo) - OFF, x.f[4 * i], a0);
-            a1 = fmaf(byte_plus_2p23<1>(lo) - OFF, x.f[4 * i + 1], a1);
-            a0 = fmaf(byte_plus_2p23<2>(lo) - OFF, x.f[4 * i + 2], a0);
-            a1 = fmaf(byte_plus_2p23<3>(lo) - OFF, x.f[4 * i + 3], a1);
-            a0 = fmaf(byte_plus_2p23<0>(hi) - OFF, x.f[16 + 4 * i], a0);
-            a1 = fmaf(byte_plus_2p23<1>(hi) - OFF, x.f[16 + 4 * i + 1], a1);
-            a0 = fmaf(byte_plus_2p23<2>(hi) - OFF, x.f[16 + 4 * i + 2], a0);
-            a1 = fmaf(byte_plus_2p23<3>(hi) - OFF, x.f[16 + 4 * i + 3], a1);
+            float l0 = byte_plus_2p23<0>(lo), l1 = byte_plus_2p23<1>(lo);
+            float l2 = byte_plus_2p23<2>(lo), l3 = byte_plus_2p23<3>(lo);
+            float h0 = byte_plus_2p23<0>(hi), h1 = byte_plus_2p23<1>(hi);
+            float h2 = byte_plus_2p23<2>(hi), h3 = byte_plus_2p23<3>(hi);
+            fadd2(l0, l1, -OFF);
+            fadd2(l2, l3, -OFF);
+            fadd2(h0, h1, -OFF);
+            fadd2(h2, h3, -OFF);
+            ffma2(a0, a1, l0, l1, x.f[4 * i], x.f[4 * i + 1]);
+            ffma2(b0, b1, l2, l3, x.f[4 * i + 2], x.f[4 * i + 3]);
+            ffma2(a0, a1, h0, h1, x.f[16 + 4 * i], x.f[16 + 4 * i + 1]);
+            ffma2(b0, b1, h2, h3, x.f[16 + 4 * i + 2], x.f[16 + 4 * i + 3]);
         }
-        return (a0 + a1) * half_bits_to_float(w.s);
+        return ((a0 + a1) + (b0 + b1)) * half_bits_to_float(w.s);
     } else if constexpr (WF == W_BF16) {
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
@@ -674,8 +679,11 @@ __device__ __forceinline__ void lds_x(XSlice<WF, XF> &x, const uint8_t *xr, int 
 // which is stored at once: no cross-warp partials and no barriers in the
 // loop.
 // ---------------------------------------------------------------------------
-template <int WF, int XF, int M>
-__global__ void __launch_bounds__(544, 1) gemv_lpr_kernel(const GemvParams p)
+// COMPACT: at most 8 consumer warps and ~48 KB of shared memory, so that
+// two CTAs of this call and two of the next fit one SM (registers capped to
+// match); used when each SM's share of the weights is small.
+template <int WF, int XF, int M, bool COMPACT>
+__global__ void __launch_bounds__(COMPACT ? 288 : 544, COMPACT ? 4 : 1) gemv_lpr_kernel(const GemvParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
@@ -799,11 +807,11 @@ __global__ void __launch_bounds__(544, 1) gemv_lpr_kernel(const GemvParams p)
     }
 }
 
-template <int WF, int XF, int M>
+template <int WF, int XF, int M, bool COMPACT>
 __host__ cudaError_t gemv_lpr_launch_one(const GemvParams &p, dim3 grid, int threads, size_t smem,
                                          cudaStream_t stream, bool pdl, int *occupancy)
 {
-    auto kern = gemv_lpr_kernel<WF, XF, M>;
+    auto kern = gemv_lpr_kernel<WF, XF, M, COMPACT>;
     if (occupancy) {
         int dev = 0, optin = 0;
         cudaFuncAttributes fa;
@@ -830,12 +838,14 @@ __host__ cudaError_t gemv_lpr_launch_one(const GemvParams &p, dim3 grid, int thr
 }
 
 template <int WF, int XF>
-__host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, int threads, size_t smem,
+__host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, bool compact, dim3 grid, int threads, size_t smem,
                                        cudaStream_t stream, bool pdl, int *occupancy)
 {
     constexpr int XR = (XF == X_BF16) ? X_F32 : XF;      // staged bf16 activations are fp32
-    if (M == 1) return gemv_lpr_launch_one<WF, XR, 1>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 2) return gemv_lpr_launch_one<WF, XR, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 1 && compact) return gemv_lpr_launch_one<WF, XR, 1, true>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 1) return gemv_lpr_launch_one<WF, XR, 1, false>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 2 && compact) return gemv_lpr_launch_one<WF, XR, 2, true>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 2) return gemv_lpr_launch_one<WF, XR, 2, false>(p, grid, threads, smem, stream, pdl, occupancy);
     return cudaErrorInvalidValue;
 }
 
