@@ -1,4 +1,29 @@
-// bqg_gemm.cu -- prefill GEMM (M = 512) on the sm_103a tensor cores.
+// bqg_gemm.cu -- prefill GEMM Y[M x N] = X[M x K] W^T on the sm_103a tensor cores.
+//
+// The tiled prefill GEMM of "llama-3x-prompt-speed" ("the tile"): a weight
+// tile is unpacked once into shared memory and serves every activation row
+// of the tile, instead of being unpacked once per row.  Here the unit of
+// work is 128 weight rows x 128 activation rows; per k-step of 64:
+//   * warps 1-4 load the q4_0 codes and scales of the 128 weight rows
+//     (repacked layout), dequantize (q - 8) * d exactly in fp32 and round
+//     once to bf16, and write a 128 x 64 bf16 tile into shared memory in the
+//     K-major 128-byte-swizzled layout the tensor core reads;
+//   * warp 0, lane 0 loads the matching 128 x 64 bf16 activation tile with
+//     one TMA copy (same swizzle) and issues four tcgen05.mma.kind::f16
+//     (M = 128 weight rows, N = 128 activations, K = 16) accumulating fp32
+//     in tensor memory; tcgen05.commit frees the stage;
+//   * warps 5-8 read the finished 128 x 128 fp32 accumulator with
+//     tcgen05.ld (each warp its 32 lanes = 32 weight rows) and store
+//     Y[m][n] coalesced along n.
+// The accumulator is double-buffered (256 TMEM columns) so the epilogue of
+// one unit overlaps the MMAs of the next.  The kernel is persistent (one
+// CTA per SM).  Every mbarrier wait is bounded: on a timeout the kernel sets
+// g_gemm_error, stops issuing work, drains what it started and frees TMEM.
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "bqg_common.cuh"
 
 namespace bqg {
@@ -6,21 +31,359 @@ namespace bqg {
 // Error word set by bounded device-side waits (0 = none).
 __device__ int g_gemm_error;
 
+namespace {
+
+constexpr int TM = 128;         // weight rows per unit (MMA M)
+constexpr int TN = 128;         // activation rows per unit (MMA N)
+constexpr int TK = 64;          // K per stage (one 128-byte swizzle atom of bf16)
+constexpr int NSTAGE = 4;
+constexpr int TILE_BYTES = TM * TK * 2;       // 16 KiB, both operands
+constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+constexpr int ACC_COLS = TN;                  // fp32 columns per accumulator
+constexpr int TMEM_COLS = 2 * ACC_COLS;       // double buffer
+constexpr int NUM_THREADS = 9 * 32;
+
+// shared memory map (dynamic, 1024-byte aligned)
+constexpr int OFF_STAGES = 0;
+constexpr int OFF_BARS = NSTAGE * STAGE_BYTES;           // mbarriers
+constexpr int NBARS = 3 * NSTAGE + 4;                    // fullW, fullX, empty per stage; acc full/empty x2
+constexpr int OFF_TMEM_SLOT = OFF_BARS + NBARS * 8;
+constexpr int OFF_FLAG = OFF_TMEM_SLOT + 8;
+constexpr int SMEM_BYTES = OFF_FLAG + 8 + 1024;          // + slack for 1024-byte alignment
+
+// instruction descriptor, kind::f16: D fp32, A bf16, B bf16, both K-major, N, M
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TN >> 3) << 17) |
+                           ((uint32_t)(TM >> 4) << 24);
+
+// K-major, 128-byte swizzle smem descriptor: rows of 128 bytes in atoms of
+// 8 rows (1024 bytes); consecutive atoms along M/N are 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3fff);            // start address
+    d |= (uint64_t)1 << 16;                            // leading byte offset (unused with swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset: next 8-row atom
+    d |= (uint64_t)1 << 46;                            // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+    return d;
+}
+
+// byte offset of 16-byte chunk c (k = 8c..8c+7) of row r in a K-major
+// 128-byte-swizzled tile
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(IDESC), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 lanes x 32 columns of fp32 from tensor memory (this warp's lane quarter)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                 "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// two fp32 -> bf16x2, round to nearest even (lo in the low half)
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 8 dequantized weights (q - 8) * d of one q4_0 word pair, as 4 bf16x2 words.
+// w0, w1 hold code bytes 4i..4i+7; `shift` 0 takes the low nibbles (elements
+// j), 4 the high nibbles (elements j + 16).
+__device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, int shift, float d)
+{
+    constexpr float OFF = 8388608.0f + 8.0f;
+    const uint32_t a = (w0 >> shift) & 0x0f0f0f0fu, b = (w1 >> shift) & 0x0f0f0f0fu;
+    float f[8] = {byte_plus_2p23<0>(a), byte_plus_2p23<1>(a), byte_plus_2p23<2>(a), byte_plus_2p23<3>(a),
+                  byte_plus_2p23<0>(b), byte_plus_2p23<1>(b), byte_plus_2p23<2>(b), byte_plus_2p23<3>(b)};
+#pragma unroll
+    for (int i = 0; i < 8; i++) f[i] = (f[i] - OFF) * d;     // exact: 4-bit integer times an fp16 value
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+struct GemmArgs {
+    const uint8_t *W;       // repacked q4_0, N rows
+    float *Y;               // M x N
+    int64_t row_bytes;      // repacked bytes per weight row
+    int M, N, K;
+    int units;              // (N / TM) * (M / TN)
+    int tiles_n;            // N / TM
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                        const GemmArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bars = sbase + OFF_BARS;
+    auto bar_fullW = [&](int s) { return bars + 8 * s; };
+    auto bar_fullX = [&](int s) { return bars + 8 * (NSTAGE + s); };
+    auto bar_empty = [&](int s) { return bars + 8 * (2 * NSTAGE + s); };
+    auto bar_accf = [&](int b) { return bars + 8 * (3 * NSTAGE + b); };
+    auto bar_acce = [&](int b) { return bars + 8 * (3 * NSTAGE + 2 + b); };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nk = a.K / TK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; s++) {
+            mbar_init(bar_fullW(s), 4);     // one arrive per dequantizing warp
+            mbar_init(bar_fullX(s), 1);     // the TMA issuer's arrive + bytes
+            mbar_init(bar_empty(s), 1);     // tcgen05.commit
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(bar_accf(b), 1);      // tcgen05.commit after a unit's last k-step
+            mbar_init(bar_acce(b), 4);      // one arrive per epilogue warp
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sbase + OFF_TMEM_SLOT),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM_SLOT);
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    auto fail = [&]() {
+        atomicExch(&g_gemm_error, 2);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ---------------- TMA issuer + MMA issuer ----------------
+        if (lane == 0) {
+            int it = 0;        // global k-step counter across units (ring position)
+            int ucount = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ucount++) {
+                const int tn = u % a.tiles_n, tm = u / a.tiles_n;      // weight tile, activation tile
+                (void)tn;
+                const int b = ucount & 1;
+                // the accumulator must have been read out (two units ago)
+                if (ucount >= 2 && !mbar_wait_bounded(bar_acce(b), ((ucount >> 1) - 1) & 1)) { fail(); ok = false; break; }
+                tc_fence_after();
+                const uint32_t dacc = tmem + b * ACC_COLS;
+                // keep up to NSTAGE activation tiles in flight ahead of the MMAs
+                int issued = it;
+                auto issue_x = [&](int step) {
+                    const int s = step % NSTAGE;
+                    const int ks = step - it;      // k-step within this unit
+                    if (step >= NSTAGE && !mbar_wait_bounded(bar_empty(s), ((step / NSTAGE) - 1) & 1)) return false;
+                    mbar_arrive_expect_tx(bar_fullX(s), TILE_BYTES);
+                    tma_load_2d(sbase + OFF_STAGES + s * STAGE_BYTES + TILE_BYTES, &xmap, ks * TK, tm * TN, bar_fullX(s));
+                    return true;
+                };
+                for (int k = 0; k < nk && ok; k++) {
+                    const int step = it + k;
+                    while (issued < it + nk && issued < step + NSTAGE) {
+                        if (!issue_x(issued)) { fail(); ok = false; break; }
+                        issued++;
+                    }
+                    if (!ok) break;
+                    const int s = step % NSTAGE;
+                    const uint32_t ph = (step / NSTAGE) & 1;
+                    if (!mbar_wait_bounded(bar_fullX(s), ph) || !mbar_wait_bounded(bar_fullW(s), ph)) {
+                        fail(); ok = false; break;
+                    }
+                    if (*abort_flag) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t aw = sbase + OFF_STAGES + s * STAGE_BYTES;       // weights: MMA A (M = 128 rows)
+                    const uint32_t bx = aw + TILE_BYTES;                            // activations: MMA B (N = 128)
+#pragma unroll
+                    for (int kk = 0; kk < TK / 16; kk++)
+                        umma_bf16(dacc, sw128_desc(aw + kk * 32), sw128_desc(bx + kk * 32), (k > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(bar_empty(s));               // stage s is free when these MMAs finish
+                }
+                if (ok) umma_commit(bar_accf(b));            // the unit's accumulator is complete
+                it += nk;
+            }
+            // drain: wait for the last MMAs before TMEM is released
+            if (it > 0) mbar_wait_bounded(bar_empty((it - 1) % NSTAGE), ((it - 1) / NSTAGE) & 1);
+        }
+        __syncwarp();
+    } else if (warp <= 4) {
+        // ---------------- weight dequantization (warps 1-4) ----------------
+        const int t = threadIdx.x - 32;                      // weight row in the unit, 0..127
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            const int tn = u % a.tiles_n;
+            const uint8_t *row = a.W + (int64_t)(tn * TM + t) * a.row_bytes;
+            for (int k = 0; k < nk; k++) {
+                const int step = it + k;
+                const int s = step % NSTAGE;
+                // this k-step's two q4_0 blocks: 32 code bytes and two fp16 scales
+                const int blk = k * 2;                       // first block of the step
+                const uint8_t *tile = row + (int64_t)(blk >> 5) * Q4_0_TILE;
+                const int slot = blk & 31;
+                const uint4 c0 = ldg_v4(tile + 16 * slot);
+                const uint4 c1 = ldg_v4(tile + 16 * (slot + 1));
+                const uint32_t sc = __ldg(reinterpret_cast<const uint32_t *>(tile + 512 + 2 * slot));
+                if (step >= NSTAGE && !mbar_wait_bounded(bar_empty(s), ((step / NSTAGE) - 1) & 1)) { fail(); ok = false; break; }
+                if (*abort_flag) { ok = false; break; }
+                const float d0 = half_bits_to_float(sc & 0xffffu), d1 = half_bits_to_float(sc >> 16);
+                uint8_t *wt = smem + OFF_STAGES + s * STAGE_BYTES;
+                // block 0: k 0..31 -> chunks 0..3; block 1: k 32..63 -> chunks 4..7
+                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 0)) = dequant8(c0.x, c0.y, 0, d0);
+                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 1)) = dequant8(c0.z, c0.w, 0, d0);
+                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 2)) = dequant8(c0.x, c0.y, 4, d0);
+                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 3)) = dequant8(c0.z, c0.w, 4, d0);
+                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 4)) = dequant8(c1.x, c1.y, 0, d1);
+                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 5)) = dequant8(c1.z, c1.w, 0, d1);
+                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 6)) = dequant8(c1.x, c1.y, 4, d1);
+                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 7)) = dequant8(c1.z, c1.w, 4, d1);
+                fence_async_smem();                          // generic-proxy writes -> tensor core reads
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_fullW(s));
+            }
+            it += nk;
+        }
+    } else {
+        // ---------------- epilogue (warps 5-8: lane quarters 1, 2, 3, 0) ----------------
+        const int quarter = warp & 3;
+        int ucount = 0;
+        for (int u = blockIdx.x; u < a.units; u += gridDim.x, ucount++) {
+            const int tn = u % a.tiles_n, tm = u / a.tiles_n;
+            const int b = ucount & 1;
+            if (*abort_flag || !mbar_wait_bounded(bar_accf(b), (ucount >> 1) & 1)) { fail(); break; }
+            tc_fence_after();
+            const int n = tn * TM + quarter * 32 + lane;     // weight row = output column
+            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + b * ACC_COLS;
+#pragma unroll 1
+            for (int c0 = 0; c0 < TN; c0 += 32) {
+                float v[32];
+                tmem_ld32(taddr + c0, v);
+#pragma unroll
+                for (int i = 0; i < 32; i++) a.Y[(int64_t)(tm * TN + c0 + i) * a.N + n] = v[i];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acce(b));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
 int gemm_read_error(cudaStream_t stream, int *out)
 {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return BQG_ERR_CUDA;
     int v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(int)) != cudaSuccess) return BQG_ERR_CUDA;
-    if (cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(int)) != cudaSuccess) return BQG_ERR_CUDA;
+    if (v && cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(int)) != cudaSuccess) return BQG_ERR_CUDA;
     *out = v;
     return BQG_OK;
 }
 
 size_t gemm_workspace(int, int64_t, int64_t) { return 0; }
 
-int gemm_q4_0_bf16(const void *, const void *, float *, int, int64_t, int64_t, cudaStream_t, int)
+// M % 128 == 0, N % 128 == 0, K % 64 == 0 (checked by the caller)
+int gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, cudaStream_t stream, int sms)
 {
-    return BQG_ERR_UNSUPPORTED_SHAPE;
+    static std::mutex mu;
+    auto enc = encode_fn();
+    if (!enc) return BQG_ERR_CUDA;
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {TK, TN};
+    const cuuint32_t estride[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(X), gdim, gstride, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return BQG_ERR_CUDA;
+    GemmArgs a;
+    a.W = static_cast<const uint8_t *>(Wp);
+    a.Y = Y;
+    const int64_t nb = K / QK, T = (nb + 31) / 32;
+    a.row_bytes = T * Q4_0_TILE;
+    a.M = M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.tiles_n = (int)(N / TM);
+    a.units = a.tiles_n * (M / TN);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        static bool attr = false;
+        if (!attr) {
+            if (cudaFuncSetAttribute(gemm_q4_0_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+                cudaSuccess)
+                return BQG_ERR_CUDA;
+            attr = true;
+        }
+    }
+    const int grid = std::min(a.units, sms);
+    gemm_q4_0_bf16_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map, a);
+    return cudaGetLastError() == cudaSuccess ? BQG_OK : BQG_ERR_CUDA;
 }
 
 }  // namespace bqg
