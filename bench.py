@@ -214,6 +214,41 @@ class GemvArm(Arm):
         return 2 * self.M * self.N * self.K
 
 
+class GemmArm(Arm):
+    """Prefill GEMM M=512 (bf16 activations) x q4_0 weights."""
+
+    def __init__(self, M=512, N=14336, K=4096, seed=9, sets=None):
+        import torch
+        import block_quantized_gemv_gb300 as bqg
+        from block_quantized_gemv_gb300 import synth
+        super().__init__()
+        self.bqg, self.M, self.N, self.K = bqg, M, N, K
+        self.name = f"q4_0 x bf16 prefill GEMM M={M} K={K} N={N}"
+        self.kernel_key = f"gemm_q4_0_bf16_M{M}_K{K}_N{N}"
+        Wf = torch.from_numpy(synth.weights_f32(N, K, seed)).cuda()
+        Wp = bqg.repack_weights(bqg.Q4_0, bqg.quantize_weights(bqg.Q4_0, Wf), N, K)
+        del Wf
+        X = torch.from_numpy(synth.activations_f32(M, K, seed + 1)).cuda().to(torch.bfloat16)
+        self.bytes_per_call = Wp.numel() + X.numel() * 2 + M * N * 4
+        self.flops = 2.0 * M * N * K
+        self.R = sets or self.rotation(self.bytes_per_call)
+        for r in range(self.R):
+            self.sets.append({"W": Wp if r == 0 else Wp.clone(), "X": X.clone(),
+                              "Y": torch.empty((M, N), dtype=torch.float32, device="cuda")})
+        self.X_host = X.cpu().pin_memory()
+        self.Y_host = torch.empty((M, N), dtype=torch.float32).pin_memory()
+
+    def call(self, i):
+        s = self.sets[i % self.R]
+        self.bqg.gemm_q4_0_bf16(s["W"], s["X"], self.N, self.K, out=s["Y"])
+
+    def call_e2e(self, i):
+        s = self.sets[i % self.R]
+        s["X"].copy_(self.X_host, non_blocking=True)
+        self.call(i)
+        self.Y_host.copy_(s["Y"], non_blocking=True)
+
+
 class DecodeLayerArm(Arm):
     """q4_0 x q8_1 decode layer: quantize(x), QKV, gate+up+SwiGLU, quantize(h), down."""
 
@@ -359,11 +394,18 @@ def arm_record(arm, t, peaks):
     calls = t["repeats"] * t["launches_per_repeat"]
     us = t["seconds"] / calls * 1e6
     gbs = gb_s(arm.bytes_per_call * calls, t["seconds"])
-    return {"workload": arm.name, "us_per_call": round(us, 3), "GB_per_s": round(gbs, 1),
-            "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_call": arm.bytes_per_call,
-            "rotating_sets": arm.R, "working_set_bytes": arm.R * arm.bytes_per_call,
-            "spread": round(t["spread"], 4), "spread_ok": t["spread_ok"],
-            "launches": calls * arm.launches_per_call}
+    rec = {"workload": arm.name, "us_per_call": round(us, 3), "GB_per_s": round(gbs, 1),
+           "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_call": arm.bytes_per_call,
+           "rotating_sets": arm.R, "working_set_bytes": arm.R * arm.bytes_per_call,
+           "spread": round(t["spread"], 4), "spread_ok": t["spread_ok"],
+           "launches": calls * arm.launches_per_call}
+    if getattr(arm, "flops", None):
+        tf = arm.flops * calls / t["seconds"] / 1e12
+        rec.update({"bound": "tensor", "TFLOP_per_s": round(tf, 1),
+                    "frac_of_tensor_peak": round(tf / peaks["bf16_tflops"], 4),
+                    "peak_note": "dense bf16 burst peak, MEASURED_PEAKS.json bf16_tflops"})
+        del rec["frac_of_peak"]
+    return rec
 
 
 # ---------------------------------------------------------------------------
@@ -411,7 +453,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--json-out", default=None)
     ap.add_argument("--min-warm-s", type=float, default=1.0, help="minimum warm-up time per arm")
-    ap.add_argument("--profile", default=None, choices=["bf16", "q8_0", "q4_0", "q4_0_q8_1"],
+    ap.add_argument("--profile", default=None, choices=["bf16", "q8_0", "q4_0", "q4_0_q8_1", "gemm"],
                     help="profiling case: only this M=1 K=4096 N=12288 arm, 2 weight sets, eager calls")
     args = ap.parse_args()
 
@@ -464,6 +506,13 @@ def main():
         pass
     sampler = NvmlSampler(uuid)
 
+    if args.profile == "gemm":
+        arm = GemmArm(sets=2)
+        for i in range(args.warmup + args.steps):
+            arm.call(i)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": arm.name, "calls": args.warmup + args.steps}))
+        return 0
     if args.profile:
         # a small case for ncu: two weight sets (cache state is ncu's to control)
         fmt = {"bf16": bqg.BF16, "q8_0": bqg.Q8_0, "q4_0": bqg.Q4_0, "q4_0_q8_1": bqg.Q4_0}[args.profile]
@@ -495,7 +544,8 @@ def main():
            "path": "pinned host x -> device, bqg_gemv_bf16 through the Python binding, y -> pinned host"}
 
     arms = [rec]
-    other = [GemvArm(bqg.Q8_0, bqg.BF16, 1, N_HEAD, K_HEAD), GemvArm(bqg.Q4_0, bqg.Q8_1, 1, N_HEAD, K_HEAD)]
+    other = [GemvArm(bqg.Q8_0, bqg.BF16, 1, N_HEAD, K_HEAD), GemvArm(bqg.Q4_0, bqg.Q8_1, 1, N_HEAD, K_HEAD),
+             GemmArm()]
     if args.suite == "full":
         other += [GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096), DecodeLayerArm()]
         for M in (1, 2, 4, 8):

@@ -107,6 +107,31 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
     return true;
 }
+// Tight variant for short pipeline waits (a few hundred cycles): plain
+// try_wait (hardware time limit), no sleep between tests; still bounded.
+__device__ __forceinline__ bool mbar_try_wait_nohint(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait_nohint(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; i++)
+            if (mbar_try_wait_nohint(bar, parity)) return true;
+        if (clock64() - t0 > kWaitTimeoutCycles) return false;
+    }
+}
+
 // Bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)

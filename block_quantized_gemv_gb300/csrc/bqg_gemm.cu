@@ -4,15 +4,15 @@
 // tile is unpacked once into shared memory and serves every activation row
 // of the tile, instead of being unpacked once per row.  Here the unit of
 // work is 128 weight rows x 128 activation rows; per k-step of 64:
-//   * warps 1-4 load the q4_0 codes and scales of the 128 weight rows
-//     (repacked layout), dequantize (q - 8) * d exactly in fp32 and round
-//     once to bf16, and write a 128 x 64 bf16 tile into shared memory in the
-//     K-major 128-byte-swizzled layout the tensor core reads;
+//   * warps 1-8 (one q4_0 block of one weight row per thread) load the codes
+//     and scale eight k-steps ahead, dequantize (q - 8) * d exactly in fp32
+//     and round once to bf16, and write the 128 x 64 bf16 tile into shared
+//     memory in the K-major 128-byte-swizzled layout the tensor core reads;
 //   * warp 0, lane 0 loads the matching 128 x 64 bf16 activation tile with
 //     one TMA copy (same swizzle) and issues four tcgen05.mma.kind::f16
 //     (M = 128 weight rows, N = 128 activations, K = 16) accumulating fp32
 //     in tensor memory; tcgen05.commit frees the stage;
-//   * warps 5-8 read the finished 128 x 128 fp32 accumulator with
+//   * warps 9-12 read the finished 128 x 128 fp32 accumulator with
 //     tcgen05.ld (each warp its 32 lanes = 32 weight rows) and store
 //     Y[m][n] coalesced along n.
 // The accumulator is double-buffered (256 TMEM columns) so the epilogue of
@@ -36,12 +36,15 @@ namespace {
 constexpr int TM = 128;         // weight rows per unit (MMA M)
 constexpr int TN = 128;         // activation rows per unit (MMA N)
 constexpr int TK = 64;          // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int NSTAGE = 4;
+constexpr int NSTAGE = 6;
 constexpr int TILE_BYTES = TM * TK * 2;       // 16 KiB, both operands
 constexpr int STAGE_BYTES = 2 * TILE_BYTES;
 constexpr int ACC_COLS = TN;                  // fp32 columns per accumulator
 constexpr int TMEM_COLS = 2 * ACC_COLS;       // double buffer
-constexpr int NUM_THREADS = 9 * 32;
+constexpr int DQ_WARPS = 8;                   // dequantizing warps (1..8)
+constexpr int EPI_WARP0 = 1 + DQ_WARPS;       // epilogue warps 9..12
+constexpr int NUM_THREADS = (EPI_WARP0 + 4) * 32;
+constexpr int PREFETCH = 8;                   // k-steps of weight codes in flight per thread
 
 // shared memory map (dynamic, 1024-byte aligned)
 constexpr int OFF_STAGES = 0;
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; s++) {
-            mbar_init(bar_fullW(s), 4);     // one arrive per dequantizing warp
+            mbar_init(bar_fullW(s), DQ_WARPS);  // one arrive per dequantizing warp
             mbar_init(bar_fullX(s), 1);     // the TMA issuer's arrive + bytes
             mbar_init(bar_empty(s), 1);     // tcgen05.commit
         }
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
                 (void)tn;
                 const int b = ucount & 1;
                 // the accumulator must have been read out (two units ago)
-                if (ucount >= 2 && !mbar_wait_bounded(bar_acce(b), ((ucount >> 1) - 1) & 1)) { fail(); ok = false; break; }
+                if (ucount >= 2 && !mbar_wait_spin(bar_acce(b), ((ucount >> 1) - 1) & 1)) { fail(); ok = false; break; }
                 tc_fence_after();
                 const uint32_t dacc = tmem + b * ACC_COLS;
                 // keep up to NSTAGE activation tiles in flight ahead of the MMAs
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
                 auto issue_x = [&](int step) {
                     const int s = step % NSTAGE;
                     const int ks = step - it;      // k-step within this unit
-                    if (step >= NSTAGE && !mbar_wait_bounded(bar_empty(s), ((step / NSTAGE) - 1) & 1)) return false;
+                    if (step >= NSTAGE && !mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1)) return false;
                     mbar_arrive_expect_tx(bar_fullX(s), TILE_BYTES);
                     tma_load_2d(sbase + OFF_STAGES + s * STAGE_BYTES + TILE_BYTES, &xmap, ks * TK, tm * TN, bar_fullX(s));
                     return true;
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
                     if (!ok) break;
                     const int s = step % NSTAGE;
                     const uint32_t ph = (step / NSTAGE) & 1;
-                    if (!mbar_wait_bounded(bar_fullX(s), ph) || !mbar_wait_bounded(bar_fullW(s), ph)) {
+                    if (!mbar_wait_spin(bar_fullX(s), ph) || !mbar_wait_spin(bar_fullW(s), ph)) {
                         fail(); ok = false; break;
                     }
                     if (*abort_flag) { ok = false; break; }
@@ -245,54 +248,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
                 it += nk;
             }
             // drain: wait for the last MMAs before TMEM is released
-            if (it > 0) mbar_wait_bounded(bar_empty((it - 1) % NSTAGE), ((it - 1) / NSTAGE) & 1);
+            if (it > 0) mbar_wait_spin(bar_empty((it - 1) % NSTAGE), ((it - 1) / NSTAGE) & 1);
         }
         __syncwarp();
-    } else if (warp <= 4) {
-        // ---------------- weight dequantization (warps 1-4) ----------------
-        const int t = threadIdx.x - 32;                      // weight row in the unit, 0..127
+    } else if (warp <= DQ_WARPS) {
+        // ---------------- weight dequantization (warps 1-8) ----------------
+        const int t = threadIdx.x - 32;
+        const int r = t & (TM - 1);                          // weight row in the unit
+        const int h = t >> 7;                                // which of the step's two blocks
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
             const int tn = u % a.tiles_n;
-            const uint8_t *row = a.W + (int64_t)(tn * TM + t) * a.row_bytes;
-            for (int k = 0; k < nk; k++) {
-                const int step = it + k;
-                const int s = step % NSTAGE;
-                // this k-step's two q4_0 blocks: 32 code bytes and two fp16 scales
-                const int blk = k * 2;                       // first block of the step
+            const uint8_t *row = a.W + (int64_t)(tn * TM + r) * a.row_bytes;
+            // block 2k + h of this row: 16 code bytes and its fp16 scale
+            auto load = [&](int k, uint4 &c, uint32_t &sc) {
+                if (k >= nk) return;
+                const int blk = 2 * k + h;
                 const uint8_t *tile = row + (int64_t)(blk >> 5) * Q4_0_TILE;
-                const int slot = blk & 31;
-                const uint4 c0 = ldg_v4(tile + 16 * slot);
-                const uint4 c1 = ldg_v4(tile + 16 * (slot + 1));
-                const uint32_t sc = __ldg(reinterpret_cast<const uint32_t *>(tile + 512 + 2 * slot));
-                if (step >= NSTAGE && !mbar_wait_bounded(bar_empty(s), ((step / NSTAGE) - 1) & 1)) { fail(); ok = false; break; }
-                if (*abort_flag) { ok = false; break; }
-                const float d0 = half_bits_to_float(sc & 0xffffu), d1 = half_bits_to_float(sc >> 16);
-                uint8_t *wt = smem + OFF_STAGES + s * STAGE_BYTES;
-                // block 0: k 0..31 -> chunks 0..3; block 1: k 32..63 -> chunks 4..7
-                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 0)) = dequant8(c0.x, c0.y, 0, d0);
-                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 1)) = dequant8(c0.z, c0.w, 0, d0);
-                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 2)) = dequant8(c0.x, c0.y, 4, d0);
-                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 3)) = dequant8(c0.z, c0.w, 4, d0);
-                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 4)) = dequant8(c1.x, c1.y, 0, d1);
-                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 5)) = dequant8(c1.z, c1.w, 0, d1);
-                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 6)) = dequant8(c1.x, c1.y, 4, d1);
-                *reinterpret_cast<uint4 *>(wt + sw128_off(t, 7)) = dequant8(c1.z, c1.w, 4, d1);
-                fence_async_smem();                          // generic-proxy writes -> tensor core reads
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_fullW(s));
+                c = ldg_v4(tile + 16 * (blk & 31));
+                sc = __ldg(reinterpret_cast<const unsigned short *>(tile + 512 + 2 * (blk & 31)));
+            };
+            // ring of PREFETCH k-steps of codes and scales in registers; the loop
+            // is unrolled by PREFETCH so each slot is reloaded right after use
+            // and never moved while its load is in flight
+            uint4 cr[PREFETCH];
+            uint32_t sr[PREFETCH];
+#pragma unroll
+            for (int i = 0; i < PREFETCH; i++) {
+                cr[i] = make_uint4(0, 0, 0, 0);
+                sr[i] = 0;
+                load(i, cr[i], sr[i]);
+            }
+            for (int k0 = 0; k0 < nk && ok; k0 += PREFETCH) {
+#pragma unroll
+                for (int i = 0; i < PREFETCH; i++) {
+                    const int k = k0 + i;
+                    if (k >= nk) break;
+                    const int step = it + k;
+                    const int s = step % NSTAGE;
+                    if (step >= NSTAGE && !mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1)) {
+                        fail(); ok = false; break;
+                    }
+                    if (*abort_flag) { ok = false; break; }
+                    const uint4 c0 = cr[i];
+                    const float d = half_bits_to_float(sr[i]);
+                    load(k + PREFETCH, cr[i], sr[i]);
+                    uint8_t *wt = smem + OFF_STAGES + s * STAGE_BYTES;
+                    // block h covers k 32h .. 32h+31 of the step: chunks 4h .. 4h+3
+                    *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 0)) = dequant8(c0.x, c0.y, 0, d);
+                    *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 1)) = dequant8(c0.z, c0.w, 0, d);
+                    *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 2)) = dequant8(c0.x, c0.y, 4, d);
+                    *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 3)) = dequant8(c0.z, c0.w, 4, d);
+                    fence_async_smem();                      // generic-proxy writes -> tensor core reads
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_fullW(s));
+                }
             }
             it += nk;
         }
     } else {
-        // ---------------- epilogue (warps 5-8: lane quarters 1, 2, 3, 0) ----------------
+        // ---------------- epilogue (warps 9-12: lane quarters 1, 2, 3, 0) ----------------
         const int quarter = warp & 3;
         int ucount = 0;
         for (int u = blockIdx.x; u < a.units; u += gridDim.x, ucount++) {
             const int tn = u % a.tiles_n, tm = u / a.tiles_n;
             const int b = ucount & 1;
-            if (*abort_flag || !mbar_wait_bounded(bar_accf(b), (ucount >> 1) & 1)) { fail(); break; }
+            if (*abort_flag || !mbar_wait_spin(bar_accf(b), (ucount >> 1) & 1)) { fail(); break; }
             tc_fence_after();
             const int n = tn * TM + quarter * 32 + lane;     // weight row = output column
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + b * ACC_COLS;
