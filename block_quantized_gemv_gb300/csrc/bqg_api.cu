@@ -19,10 +19,10 @@ cudaError_t gemv_error_bf16(int *);
 cudaError_t gemv_error_q8_0(int *);
 cudaError_t gemv_error_q4_0(int *);
 cudaError_t gemv_error_q4_0_q8_1(int *);
-cudaError_t gemv_lpr_run_bf16(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
-cudaError_t gemv_lpr_run_q8_0(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
-cudaError_t gemv_lpr_run_q4_0(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
-cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_bf16(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q8_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q4_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 int gemv_x_stage_bytes_bf16(int, int);
 int gemv_x_stage_bytes_q8_0(int, int);
 int gemv_x_stage_bytes_q4_0(int, int);
@@ -114,7 +114,7 @@ RunFn runner(int wf, int xf)
     return gemv_run_q4_0;
 }
 
-using LprFn = cudaError_t (*)(const GemvParams &, int, bool, dim3, int, size_t, cudaStream_t, bool, int *);
+using LprFn = cudaError_t (*)(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 LprFn lpr_runner(int wf, int xf)
 {
     if (xf == X_Q8_1) return gemv_lpr_run_q4_0_q8_1;
@@ -132,14 +132,14 @@ int x_stage_bytes(int wf, int xf, int nc, int nb)
 
 struct GemvPlan {
     bool lpr;               // lanes-per-row kernel (M <= 2)
-    bool compact;           // its compact configuration (small weight share per SM)
-    int L, x_off, x_row_bytes, wg, ng;
+    int L, x_off, x_row_bytes, xraw_off, early, rl, piece_chunks, wg, ng;
     int C, TPR, RG, RPS, nc, cps, splits, threads, ncons, S, NS, stride, win_stages, part_off, bar_off, ctas;
     dim3 grid;
     size_t smem, ws_bytes;
 };
 
 constexpr int kMaxK = 65536;
+constexpr int kLprMaxWarps = 12;       // the lanes-per-row kernel's launch bound: 384 threads
 // Staged weights per CTA.  Two CTAs per SM stream a GEMV; when one of them
 // finishes, the next GEMV's CTA takes its place and starts its own weight
 // stream while the other drains (programmatic dependent launch).
@@ -148,8 +148,9 @@ constexpr int kStageBudget = 100 * 1024;
 // Tuning knobs read once from the environment (unset = defaults above):
 //   BQG_STAGE_KB     staged-weight budget per CTA in KiB
 //   BQG_CTAS_PER_SM  cap on resident GEMV CTAs per SM (1 or 2)
-//   BQG_COMPACT_KB   run the compact lanes-per-row configuration when each
-//                    SM's weight share is at most this many KiB (default 0)
+//   BQG_LPR_KB, BQG_LPR_OVERLAP_KB, BQG_OVERLAP_SHARE_KB, BQG_LPR_L, BQG_LPR_D,
+//   BQG_LPR_EARLY, BQG_LPR_RL, BQG_LPR_PIECE, BQG_LPR_STAGE_KB
+//                    lanes-per-row geometry (see plan_lpr)
 //   BQG_NO_LPR       1: serve M <= 2 with the K-slice kernel
 int env_int(const char *name, int dflt)
 {
@@ -254,12 +255,28 @@ int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevI
 // Launch geometry of the lanes-per-row kernel (M <= 2).  Returns
 // BQG_ERR_UNSUPPORTED_SHAPE when the staged activations would not fit, in
 // which case the K-slice kernel (plan_gemv) serves the call.
+//
+// Two CTAs per SM stream the call, each with about half of the SM's shared
+// memory.  An optional "overlap" geometry (BQG_OVERLAP_SHARE_KB > 0: SMs
+// whose weight share is at most that many KiB) keeps each CTA to a quarter
+// of the SM so that the next call's CTAs can be resident while this call
+// drains; measured on the decode shapes it loses more to the smaller
+// per-CTA ring and warp count than it gains, so it is off by default.
 int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevInfo &dev, int device,
              GemvPlan *pl)
 {
     if (M > 2) return BQG_ERR_UNSUPPORTED_SHAPE;
     static const bool off = env_int("BQG_NO_LPR", 0) != 0;
     if (off) return BQG_ERR_UNSUPPORTED_SHAPE;
+    static const int big_kb = std::max(16, std::min(220, env_int("BQG_LPR_KB", 110)));
+    static const int small_kb = std::max(16, std::min(110, env_int("BQG_LPR_OVERLAP_KB", 54)));
+    static const int share_kb = env_int("BQG_OVERLAP_SHARE_KB", 0);       // measured: off
+    static const int force_L = env_int("BQG_LPR_L", 0);
+    static const int force_D = env_int("BQG_LPR_D", 0);
+    static const int early = std::max(0, env_int("BQG_LPR_EARLY", 1));
+    static const int force_rl = env_int("BQG_LPR_RL", 0);
+    static const int force_pg = env_int("BQG_LPR_PIECE", 0);
+    static const int max_stage_kb = std::max(1, env_int("BQG_LPR_STAGE_KB", 16));
     GemvPlan g{};
     g.lpr = true;
     g.nc = chunk_space(wf, K);
@@ -269,53 +286,68 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     g.splits = 1;
     if (Nv < (int64_t)dev.sms * 4)
         g.splits = (int)std::min<int64_t>(maxs, ((int64_t)dev.sms * 4 + Nv - 1) / std::max<int64_t>(Nv, 1));
-    for (;;) {
-        g.cps = g.nc;
-        if (g.splits > 1) {
-            g.cps = ((g.nc + g.splits - 1) / g.splits + align - 1) / align * align;
-            g.splits = (g.nc + g.cps - 1) / g.cps;
-        }
-        g.stride = (int)range_bytes(wf, g.cps);
-        if (2ll * g.stride <= stage_budget()) break;
-        if (g.splits >= maxs) return BQG_ERR_UNSUPPORTED_SHAPE;
-        g.splits++;
+    g.x_row_bytes = (x_stage_bytes(wf, xf, g.nc, nb) + 15) / 16 * 16;
+    // staged activations plus their raw copy (the 16-byte-aligned span
+    // around X: up to 15 bytes of slack on either side)
+    const int xraw = (int)((M * ((xf == X_Q8_1) ? (int64_t)nb * Q8_1_BYTES : K * 2) + 30) / 16 * 16);
+    const int xbytes = M * g.x_row_bytes + xraw + 16;
+    if (xbytes > 64 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
+    g.cps = g.nc;
+    if (g.splits > 1) {
+        g.cps = ((g.nc + g.splits - 1) / g.splits + align - 1) / align * align;
+        g.splits = (g.nc + g.cps - 1) / g.cps;
     }
-    // A small weight share per SM runs the compact configuration, which lets
-    // the next call's CTAs share the SM and start streaming early.
+    g.stride = (int)range_bytes(wf, g.cps);          // bytes of a row's split range
+    // A warp works on RL rows at a time with all 32 lanes (gate/up blocks
+    // need an even RL); every activation load serves the RL rows.  The rows
+    // stream in K-pieces of whole tiles: the whole split range when RL rows
+    // of it fit in `max_stage` bytes, so that each stage is one bulk copy of
+    // consecutive rows (the copy engine costs about as much per copy as per
+    // few KiB moved).
+    g.L = 32;
+    // measured on the decode shapes: two rows per warp for q4_0 x q8_1 (its
+    // rows are short, so the copy stays large), one row for the others
+    int rl = (M == 1 && xf == X_Q8_1) ? 2 : 1;
+    if (force_rl == 1 || force_rl == 2 || (force_rl == 4 && M == 1)) rl = force_rl;
+    if (unit == 2 && (rl & 1)) rl = 2;
+    g.rl = rl;
+    g.wg = 1;
+    g.S = rl;
+    const int cpt = (wf == W_Q8_0) ? 64 : 32;                        // chunks per tile
+    const int64_t tile_bytes = (wf == W_Q8_0) ? Q8_0_TILE : (wf == W_Q4_0) ? Q4_0_TILE : 512;
     const int64_t per_sm = Nv * (int64_t)g.stride * g.splits / std::max(1, dev.sms);
-    static const int compact_kb = env_int("BQG_COMPACT_KB", 0);   // off unless asked for
-    g.compact = per_sm <= (int64_t)compact_kb * 1024;
-    const int budget = g.compact ? 44 * 1024 : stage_budget();
-    const int max_warps = g.compact ? 8 : 16;
-    // lanes per row: at least eight chunks per lane; gate/up pairs need two rows per warp
-    g.L = (g.cps >= 256) ? 32 : (g.cps >= 128) ? 16 : 8;
-    if (unit == 2 && g.L == 32) g.L = 16;
-    const int R = 32 / g.L;
-    // stages of about 16 KiB, a whole number of warps' rows
-    int rows = std::max(1, (int)(16384 / g.stride));
-    rows = std::max(R, rows / R * R);
-    g.S = rows;
-    const int wg = g.S / R;
-    g.NS = (int)std::max<int64_t>(2, std::min<int64_t>(16, budget / ((int64_t)g.S * g.stride)));
-    const int ng = std::max(1, std::min(g.NS, max_warps / wg));
-    if (wg > max_warps) return BQG_ERR_UNSUPPORTED_SHAPE;
-    g.wg = wg;
+    const bool overlap = per_sm <= (int64_t)share_kb * 1024;
+    const int64_t budget = (int64_t)(overlap ? small_kb : big_kb) * 1024 - xbytes - 1024;
+    const int max_tiles = (g.cps + cpt - 1) / cpt;
+    int ntile = (int)std::max<int64_t>(1, (int64_t)max_stage_kb * 1024 / ((int64_t)g.S * tile_bytes));
+    ntile = std::min(ntile, max_tiles);
+    if (force_pg > 0) ntile = std::min(force_pg, max_tiles);
+    g.piece_chunks = ntile * cpt;
+    g.stride = (int)range_bytes(wf, std::min(g.piece_chunks, g.cps));
+    const int64_t stage = (int64_t)g.S * g.stride;
+    if (budget < stage) return BQG_ERR_UNSUPPORTED_SHAPE;
+    const int max_warps = overlap ? 8 : kLprMaxWarps;
+    const int slots = (int)std::min<int64_t>(64, budget / stage);
+    int ng = std::max(1, std::min(max_warps, slots / 2));
+    int D = std::max(1, slots / ng);
+    if (force_D > 0) { D = force_D; ng = std::max(1, std::min(max_warps, slots / D)); }
     g.ng = ng;
-    g.TPR = 32 * wg * ng;
+    g.NS = D;
+    g.TPR = 32 * g.ng;
     g.RG = 1;
     g.C = 1;
     g.ncons = g.TPR;
-    g.threads = g.ncons + 32;
-    g.x_row_bytes = (x_stage_bytes(wf, xf, g.nc, nb) + 15) / 16 * 16;
-    if ((int64_t)M * g.x_row_bytes > 48 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
-    g.x_off = g.NS * g.S * g.stride;
-    g.bar_off = (g.x_off + M * g.x_row_bytes + 15) / 16 * 16;
-    g.smem = (size_t)g.bar_off + 16 * g.NS;
+    g.threads = g.TPR;
+    g.x_off = (int)(g.ng * (int64_t)D * stage);
+    g.xraw_off = (g.x_off + M * g.x_row_bytes + 15) / 16 * 16;
+    g.bar_off = (int)(g.xraw_off + xraw);
+    g.smem = (size_t)g.bar_off + 8 * (g.ng * D + 1);
+    g.early = std::min(D, early);
     if (g.smem > 232448) return BQG_ERR_UNSUPPORTED_SHAPE;
 
     int bpsm = 0;
     {
-        auto key = std::make_tuple(device, wf, xf, M, g.compact ? 1 : 0, g.threads, 1, g.smem);
+        auto key = std::make_tuple(device, wf, xf, M, g.rl, g.threads, 1, g.smem);
         std::unique_lock<std::mutex> lk(g_mu);
         auto it = g_occ.find(key);
         if (it != g_occ.end()) {
@@ -323,7 +355,8 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
         } else {
             lk.unlock();
             GemvParams dummy{};
-            const cudaError_t e = lpr_runner(wf, xf)(dummy, M, g.compact, dim3(1), g.threads, g.smem, 0, false, &bpsm);
+            dummy.rl = g.rl;
+            const cudaError_t e = lpr_runner(wf, xf)(dummy, M, dim3(1), g.threads, g.smem, 0, false, &bpsm);
             if (e != cudaSuccess) return cuda_status(e);
             lk.lock();
             g_occ[key] = bpsm;
@@ -384,11 +417,15 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     p.wg = g.wg;
     p.ng = g.ng;
     p.x_off = g.x_off;
+    p.xraw_off = g.xraw_off;
+    p.early = g.early;
+    p.rl = g.rl;
+    p.piece_chunks = g.piece_chunks;
     p.x_row_bytes = g.x_row_bytes;
     p.ws = (float *)ws;
     p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;
     const bool pdl = g_pdl.load() != 0;
-    cudaError_t e = g.lpr ? lpr_runner(wf, xf)(p, M, g.compact, g.grid, g.threads, g.smem, stream, pdl, nullptr)
+    cudaError_t e = g.lpr ? lpr_runner(wf, xf)(p, M, g.grid, g.threads, g.smem, stream, pdl, nullptr)
                           : runner(wf, xf)(p, M, g.C, g.grid, g.threads, g.smem, stream, pdl, nullptr);
     if (e != cudaSuccess) return cuda_status(e);
     if (g.splits > 1) {

@@ -132,6 +132,10 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity)
     }
 }
 
+// Order this thread's generic-proxy shared-memory accesses before its later
+// async-proxy ones (bulk copies, tensor-core operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)

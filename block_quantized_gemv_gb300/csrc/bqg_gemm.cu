@@ -98,7 +98,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar)
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // 32 lanes x 32 columns of fp32 from tensor memory (this warp's lane quarter)
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
@@ -300,7 +299,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
                     *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 1)) = dequant8(c0.z, c0.w, 0, d);
                     *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 2)) = dequant8(c0.x, c0.y, 4, d);
                     *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 3)) = dequant8(c0.z, c0.w, 4, d);
-                    fence_async_smem();                      // generic-proxy writes -> tensor core reads
+                    fence_proxy_async_smem();                      // generic-proxy writes -> tensor core reads
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_fullW(s));
                 }

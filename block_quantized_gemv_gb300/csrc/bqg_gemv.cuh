@@ -72,6 +72,10 @@ struct GemvParams {
     int ng;                 // stage groups
     int x_off;              // byte offset of the staged activations
     int x_row_bytes;        // staged bytes of one activation row
+    int xraw_off;           // byte offset of the raw activation copy (lanes-per-row kernel)
+    int early;              // stages per warp requested before waiting for the previous grid
+    int rl;                 // rows per lane (lanes-per-row kernel: 1, 2 or 4)
+    int piece_chunks;       // chunks per K-piece (lanes-per-row kernel)
 };
 
 // Error word set when a bounded wait gives up (one per translation unit).
@@ -372,12 +376,41 @@ __device__ __forceinline__ int64_t staged_vrow(const GemvParams &p, int64_t vs, 
     return vs + r;
 }
 
-// The producer lane: streams stages [0, nst) of this CTA's rows into the
-// ring with cp.async.bulk, one copy per run of consecutive rows of one
-// matrix.  The first NS stages are requested before waiting for the
-// previous grid on the stream: weights do not depend on it (the documented
-// contract of programmatic dependent launch), so this call's weight stream
-// overlaps the previous kernel's tail.
+// Fill one stage: the staged rows of the stage that starts at virtual row vs
+// (those below v1), one cp.async.bulk per run of consecutive rows of one
+// matrix, all completing on `bar`, which is told the byte count first.
+template <int WF>
+__device__ __forceinline__ void issue_stage(const GemvParams &p, uint32_t dst, uint32_t bar, int64_t vs, int S,
+                                            int64_t v1, int64_t roff, int64_t rbytes)
+{
+    const bool whole_rows = (roff == 0 && rbytes == p.row_bytes);
+    int nvalid = 0;
+    for (int r = 0; r < S; r++) nvalid += staged_vrow(p, vs, S, r) < v1;
+    mbar_arrive_expect_tx(bar, (uint32_t)(nvalid * rbytes));
+    for (int r = 0; r < S;) {
+        const int64_t v = staged_vrow(p, vs, S, r);
+        if (v >= v1) { r++; continue; }
+        int mat; int64_t rr;
+        map_row(p, v, mat, rr);
+        int len = 1;
+        while (whole_rows && r + len < S) {
+            const int64_t vn = staged_vrow(p, vs, S, r + len);
+            if (vn >= v1) break;
+            int mn; int64_t rn;
+            map_row(p, vn, mn, rn);
+            if (mn != mat || rn != rr + len) break;
+            len++;
+        }
+        bulk_g2s(dst + r * p.row_stride, p.W[mat] + rr * p.row_bytes + roff, (uint32_t)(len * rbytes), bar);
+        r += len;
+    }
+}
+
+// The producer lane of the K-slice kernel: streams stages [0, nst) of this
+// CTA's rows into the ring.  The first NS stages are requested before
+// waiting for the previous grid on the stream: weights do not depend on it
+// (the documented contract of programmatic dependent launch), so this call's
+// weight stream overlaps the previous kernel's tail.
 template <int WF>
 __device__ __forceinline__ void produce_stages(const GemvParams &p, uint8_t *smem, uint32_t bar0, int64_t v0,
                                                int64_t v1, int64_t roff, int64_t rbytes, int nst, int *s_abort)
@@ -385,7 +418,6 @@ __device__ __forceinline__ void produce_stages(const GemvParams &p, uint8_t *sme
     const int S = p.stage_rows;
     const int NS = p.nstages;
     const int stage_bytes = S * p.row_stride;
-    const bool whole_rows = (roff == 0 && rbytes == p.row_bytes);
     int s = 0;
     uint32_t ph = 0;
     int issued = 0;
@@ -397,29 +429,8 @@ __device__ __forceinline__ void produce_stages(const GemvParams &p, uint8_t *sme
             break;
         }
         if (*(volatile int *)s_abort) break;
-        const int64_t vs = v0 + (int64_t)j * S;
-        const uint32_t dst = smem_u32(smem) + (uint32_t)(s * stage_bytes);
-        int nvalid = 0;
-        for (int r = 0; r < S; r++) nvalid += staged_vrow(p, vs, S, r) < v1;
-        mbar_arrive_expect_tx(bar0 + 8 * s, (uint32_t)(nvalid * rbytes));
-        for (int r = 0; r < S;) {
-            const int64_t v = staged_vrow(p, vs, S, r);
-            if (v >= v1) { r++; continue; }
-            int mat; int64_t rr;
-            map_row(p, v, mat, rr);
-            int len = 1;
-            while (whole_rows && r + len < S) {
-                const int64_t vn = staged_vrow(p, vs, S, r + len);
-                if (vn >= v1) break;
-                int mn; int64_t rn;
-                map_row(p, vn, mn, rn);
-                if (mn != mat || rn != rr + len) break;
-                len++;
-            }
-            bulk_g2s(dst + r * p.row_stride, p.W[mat] + rr * p.row_bytes + roff, (uint32_t)(len * rbytes),
-                     bar0 + 8 * s);
-            r += len;
-        }
+        issue_stage<WF>(p, smem_u32(smem) + (uint32_t)(s * stage_bytes), bar0 + 8 * s, v0 + (int64_t)j * S, S, v1,
+                        roff, rbytes);
         issued = j + 1;
         if (++s == NS) { s = 0; ph ^= 1; }
     }
@@ -645,6 +656,47 @@ __device__ __forceinline__ void stage_x(const GemvParams &p, uint8_t *xs, int M,
     }
 }
 
+// Bytes of one activation row as the caller passes it: q8_1 blocks, or bf16
+// (staged as fp32).
+template <int XF>
+__device__ __forceinline__ int64_t x_src_row_bytes(const GemvParams &p)
+{
+    return (XF == X_Q8_1) ? (int64_t)p.nb * Q8_1_BYTES : (int64_t)p.K * 2;
+}
+
+// The same staged layout as stage_x, built from a raw copy of the M
+// activation rows in shared memory (`raw` points at X[0]).
+template <int WF, int XF>
+__device__ __forceinline__ void expand_x(const GemvParams &p, const uint8_t *raw, uint8_t *xs, int M, int tid, int nthr)
+{
+    constexpr int P = XPieces<WF, XF>::P;
+    const int runs = (p.nc + 31) / 32;
+    for (int m = 0; m < M; m++) {
+        uint8_t *xr = xs + (size_t)m * p.x_row_bytes;
+        for (int i = tid; i < p.nc * P; i += nthr) {
+            const int c = i / P, pc = i - (i / P) * P;
+            if (!chunk_valid<WF>(c, p.nb, p.nc)) continue;
+            uint4 v;
+            if constexpr (XF == X_Q8_1) {
+                const uint32_t *blk = reinterpret_cast<const uint32_t *>(raw + ((int64_t)m * p.nb + c) * Q8_1_BYTES);
+                v = make_uint4(blk[1 + 4 * pc], blk[2 + 4 * pc], blk[3 + 4 * pc], blk[4 + 4 * pc]);
+                if (pc == 0) {
+                    int sum = 0;
+#pragma unroll
+                    for (int k = 0; k < 8; k++) sum = __dp4a((int)blk[1 + k], 0x01010101, sum);
+                    const float2 ds = make_float2(half_bits_to_float(blk[0] & 0xffffu), __int_as_float(sum));
+                    *reinterpret_cast<float2 *>(xr + (size_t)runs * P * 512 + (size_t)c * 8) = ds;
+                }
+            } else {
+                // four consecutive bf16 -> fp32
+                const uint2 w = *reinterpret_cast<const uint2 *>(raw + ((int64_t)m * p.K + chunk_elem0<WF>(c) + 4 * pc) * 2);
+                v = make_uint4(w.x << 16, w.x & 0xffff0000u, w.y << 16, w.y & 0xffff0000u);
+            }
+            *reinterpret_cast<uint4 *>(xr + ((size_t)(c >> 5) * P + pc) * 512 + (c & 31) * 16) = v;
+        }
+    }
+}
+
 template <int WF, int XF>
 __device__ __forceinline__ void lds_x(XSlice<WF, XF> &x, const uint8_t *xr, int c, int runs)
 {
@@ -668,150 +720,394 @@ __device__ __forceinline__ void lds_x(XSlice<WF, XF> &x, const uint8_t *xr, int 
 }
 
 // ---------------------------------------------------------------------------
-// Lanes-per-row kernel (M = 1, 2).  The producer warp streams small stages
-// of rows into the same shared-memory ring as gemv_kernel.  Consumer warps
-// form NG groups of WG warps; group g takes stages g, g + NG, ... so many
-// warps work while each stage stays small.  Within a stage every warp takes
-// R = 32/L rows; the L lanes of a row walk its K range (chunks sub,
-// sub + L, ...) in a tight loop, reading weights from the staged row and
-// activations from a shared-memory copy made once per CTA, and accumulate
-// one register per output.  One L-lane shuffle reduction finishes each row,
-// which is stored at once: no cross-warp partials and no barriers in the
-// loop.
+// Tile loops of the lanes-per-row kernel.  A "tile" is 32 lane units of a
+// row: 32 q8_0 / q4_0 blocks (one repacked tile) or 32 chunks of 8 bf16.
+// Lane `sub` owns unit `sub` of every tile, so all its addresses inside a
+// tile are fixed offsets from the tile's base; the staged activations use
+// the matching layout (16-byte piece pc of unit s of tile t at
+// t * TX + pc * 512 + s * 16), which keeps every warp-wide shared load
+// conflict-free.  Sums go to two fp32 partials per output (acc[i][m][0..1]).
 // ---------------------------------------------------------------------------
-// COMPACT: at most 8 consumer warps and ~48 KB of shared memory, so that
-// two CTAs of this call and two of the next fit one SM (registers capped to
-// match); used when each SM's share of the weights is small.
-template <int WF, int XF, int M, bool COMPACT>
-__global__ void __launch_bounds__(COMPACT ? 288 : 544, COMPACT ? 4 : 1) gemv_lpr_kernel(const GemvParams p)
+template <int WF> struct TileTraits;
+template <> struct TileTraits<W_BF16> { static constexpr int CPT = 32, TW = 512; };    // chunks, weight bytes
+template <> struct TileTraits<W_Q8_0> { static constexpr int CPT = 64, TW = Q8_0_TILE; };
+template <> struct TileTraits<W_Q4_0> { static constexpr int CPT = 32, TW = Q4_0_TILE; };
+// staged activation bytes of one tile
+template <int WF, int XF> struct TileX { static constexpr int TX = (WF == W_BF16) ? 1024 : 4096; };
+template <> struct TileX<W_Q4_0, X_Q8_1> { static constexpr int TX = 1024; };
+
+// sum over the 16 int8 codes of c of q * x (x: 16 fp32 in four float4), into
+// four running partials
+__device__ __forceinline__ void q8x16(const uint4 &c, const float4 *x, float &a0, float &a1, float &b0, float &b1)
+{
+    constexpr float OFF = 8388608.0f + 128.0f;     // codes enter as 2^23 + (q + 128)
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const uint32_t u = cw[k] ^ 0x80808080u;
+        float e0 = byte_plus_2p23<0>(u), e1 = byte_plus_2p23<1>(u);
+        float e2 = byte_plus_2p23<2>(u), e3 = byte_plus_2p23<3>(u);
+        fadd2(e0, e1, -OFF);
+        fadd2(e2, e3, -OFF);
+        ffma2(a0, a1, e0, e1, x[k].x, x[k].y);
+        ffma2(b0, b1, e2, e3, x[k].z, x[k].w);
+    }
+}
+
+// sum over 32 q4_0 codes (16 bytes: word k = elements 4k..4k+3 in its low
+// nibbles, 16+4k..16+4k+3 in its high nibbles) of (q - 8) * x, x: 32 fp32
+__device__ __forceinline__ float q4x32(const uint4 &c, const float4 *x)
+{
+    constexpr float OFF = 8388608.0f + 8.0f;
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const uint32_t lo = cw[k] & 0x0f0f0f0fu;
+        const uint32_t hi = (cw[k] >> 4) & 0x0f0f0f0fu;
+        float l0 = byte_plus_2p23<0>(lo), l1 = byte_plus_2p23<1>(lo);
+        float l2 = byte_plus_2p23<2>(lo), l3 = byte_plus_2p23<3>(lo);
+        float h0 = byte_plus_2p23<0>(hi), h1 = byte_plus_2p23<1>(hi);
+        float h2 = byte_plus_2p23<2>(hi), h3 = byte_plus_2p23<3>(hi);
+        fadd2(l0, l1, -OFF);
+        fadd2(l2, l3, -OFF);
+        fadd2(h0, h1, -OFF);
+        fadd2(h2, h3, -OFF);
+        ffma2(a0, a1, l0, l1, x[k].x, x[k].y);
+        ffma2(b0, b1, l2, l3, x[k].z, x[k].w);
+        ffma2(a0, a1, h0, h1, x[4 + k].x, x[4 + k].y);
+        ffma2(b0, b1, h2, h3, x[4 + k].z, x[4 + k].w);
+    }
+    return (a0 + a1) + (b0 + b1);
+}
+
+// four unsigned bytes of a times four signed bytes of b, plus c
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// exact sum over 32 q4_0 codes of (q - 8) * qx: low nibbles against codes
+// 0..15 of the q8_1 block, high nibbles (kept as 16 h, unsigned) against
+// codes 16..31; the second sum is a multiple of 16 and divides exactly
+__device__ __forceinline__ int q4q8_sumi(const uint4 &c, const uint4 &xlo, const uint4 &xhi, int xsum)
+{
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    const int xl[4] = {(int)xlo.x, (int)xlo.y, (int)xlo.z, (int)xlo.w};
+    const int xh[4] = {(int)xhi.x, (int)xhi.y, (int)xhi.z, (int)xhi.w};
+    int a = 0, b = 0;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        a = __dp4a((int)(cw[k] & 0x0f0f0f0fu), xl[k], a);
+        b = dp4a_us(cw[k] & 0xf0f0f0f0u, xh[k], b);
+    }
+    return a + (b >> 4) - 8 * xsum;
+}
+
+// acc[i][m] += dot(row i of the stage, activation row m) over tiles
+// [0, nt) of the stage (global tile tg + t); in the last tile only lanes
+// below `tail` hold a unit.
+template <int WF, int XF, int M, int RL>
+__device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t *stage, int row_stride,
+                                          const uint8_t *xs, int x_row_bytes, int ds_off, int tg, int nt, int tail,
+                                          int sub)
+{
+    constexpr int TW = TileTraits<WF>::TW;
+    constexpr int TX = TileX<WF, XF>::TX;
+    const uint8_t *w0 = stage + 16 * sub;
+    const uint8_t *x0 = xs + (int64_t)tg * TX + 16 * sub;
+    auto body = [&](int t) {
+        const uint8_t *wt = w0 + t * TW;
+        const uint8_t *xt = x0 + t * TX;
+        if constexpr (WF == W_BF16) {
+            uint4 c[RL];
+#pragma unroll
+            for (int i = 0; i < RL; i++) c[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride);
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                const float4 xa = *reinterpret_cast<const float4 *>(xt + m * x_row_bytes);
+                const float4 xb = *reinterpret_cast<const float4 *>(xt + m * x_row_bytes + 512);
+#pragma unroll
+                for (int i = 0; i < RL; i++) {
+                    float &s0 = acc[i][m][0], &s1 = acc[i][m][1];
+                    ffma2(s0, s1, bf16_lo(c[i].x), bf16_hi(c[i].x), xa.x, xa.y);
+                    ffma2(s0, s1, bf16_lo(c[i].y), bf16_hi(c[i].y), xa.z, xa.w);
+                    ffma2(s0, s1, bf16_lo(c[i].z), bf16_hi(c[i].z), xb.x, xb.y);
+                    ffma2(s0, s1, bf16_lo(c[i].w), bf16_hi(c[i].w), xb.z, xb.w);
+                }
+            }
+        } else if constexpr (WF == W_Q8_0) {
+            // unit = block sub: codes 0..15 at +0, 16..31 at +512, scale at 1024 + 2 sub
+            uint4 c0[RL], c1[RL];
+            float d[RL];
+#pragma unroll
+            for (int i = 0; i < RL; i++) {
+                c0[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride);
+                c1[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride + 512);
+                d[i] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(wt + i * row_stride + 1024 - 14 * sub));
+            }
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                float4 x[8];
+#pragma unroll
+                for (int pc = 0; pc < 8; pc++) x[pc] = *reinterpret_cast<const float4 *>(xt + m * x_row_bytes + pc * 512);
+#pragma unroll
+                for (int i = 0; i < RL; i++) {
+                    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+                    q8x16(c0[i], x, a0, a1, b0, b1);
+                    q8x16(c1[i], x + 4, a0, a1, b0, b1);
+                    acc[i][m][0] = fmaf((a0 + a1) + (b0 + b1), d[i], acc[i][m][0]);
+                }
+            }
+        } else if constexpr (XF == X_Q8_1) {
+            // unit = block sub: codes at +0, scale at 512 + 2 sub; q8_1 codes at +0 / +512, (d, sum) at ds_off
+            uint4 c[RL];
+            float d[RL];
+#pragma unroll
+            for (int i = 0; i < RL; i++) {
+                c[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride);
+                d[i] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(wt + i * row_stride + 512 - 14 * sub));
+            }
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                const uint4 xl = *reinterpret_cast<const uint4 *>(xt + m * x_row_bytes);
+                const uint4 xh = *reinterpret_cast<const uint4 *>(xt + m * x_row_bytes + 512);
+                const float2 ds = *reinterpret_cast<const float2 *>(xs + m * x_row_bytes + ds_off +
+                                                                    ((tg + t) * 32 + sub) * 8);
+#pragma unroll
+                for (int i = 0; i < RL; i++)
+                    acc[i][m][0] = fmaf(d[i] * ds.x, (float)q4q8_sumi(c[i], xl, xh, __float_as_int(ds.y)),
+                                        acc[i][m][0]);
+            }
+        } else {
+            // q4_0 against fp32 activations: unit = block sub
+            uint4 c[RL];
+            float d[RL];
+#pragma unroll
+            for (int i = 0; i < RL; i++) {
+                c[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride);
+                d[i] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(wt + i * row_stride + 512 - 14 * sub));
+            }
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                float4 x[8];
+#pragma unroll
+                for (int pc = 0; pc < 8; pc++) x[pc] = *reinterpret_cast<const float4 *>(xt + m * x_row_bytes + pc * 512);
+#pragma unroll
+                for (int i = 0; i < RL; i++) acc[i][m][0] = fmaf(q4x32(c[i], x), d[i], acc[i][m][0]);
+            }
+        }
+    };
+    int t = 0;
+#pragma unroll 2
+    for (; t + 1 < nt; t++) body(t);
+    if (nt > 0 && sub < tail) body(nt - 1);
+}
+
+// ---------------------------------------------------------------------------
+// Lanes-per-row kernel (M = 1, 2).  There is no producer warp: each of the
+// CTA's NW warps streams its own work.  The CTA's rows are cut into blocks
+// of RL consecutive rows (a gate/up block holds RL/2 gate rows, then the
+// matching up rows), and block b belongs to warp b % NW.  A block is
+// streamed in K-pieces of whole tiles: stage (b, piece) holds that piece of
+// the block's rows, one bulk copy per run of rows.  Each warp owns D
+// shared-memory slots and uses them in turn.  Lane 0 requests the warp's
+// first stages before the grid waits for the previous kernel on the stream
+// (weights do not depend on it) and refills a slot with the warp's stage D
+// places later as soon as the warp has read it.  A slot is only ever filled
+// and read by its own warp, in order, so each full barrier is waited on once
+// per phase and no empty barrier is needed.
+//
+// All 32 lanes of the warp work on every row of the block (lpr_tiles): each
+// activation load serves the RL rows.  Sums carry across the pieces of a
+// block; after its last piece one warp shuffle reduction per output
+// finishes the block, which lane 0 stores.
+// ---------------------------------------------------------------------------
+template <int WF, int XF, int M, int RL>
+__global__ void __launch_bounds__(384, 2) gemv_lpr_kernel(const GemvParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
+    constexpr int CPT = TileTraits<WF>::CPT;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int ncons = p.TPR;                       // consumer threads = 32 * NG * WG
-    const int S = p.stage_rows;                    // WG * R rows per stage
-    const int NS = p.nstages;
-    const int stage_bytes = S * p.row_stride;
+    const int NW = p.ng;                           // warps
+    const int D = p.nstages;                       // slots per warp
+    const int PCS = p.piece_chunks;                // chunks per K-piece (whole tiles)
+    const int row_stride = p.row_stride;           // bytes of one row's piece
+    const int stage_bytes = RL * row_stride;
     uint8_t *xs = smem + p.x_off;
-    const uint32_t bar0 = smem_u32(smem + p.bar_off);
+    const uint32_t bar0 = smem_u32(smem + p.bar_off);      // full barriers (NW * D), then the activation copy's
 
     int64_t v0, v1;
     cta_rows(p, v0, v1);
     const int split = blockIdx.y;
     const int cbeg = split * p.chunks_per_split;
     const int cend = min(p.nc, cbeg + p.chunks_per_split);
-    int64_t roff, rbytes;
-    chunk_range_bytes<WF>(cbeg, cend, roff, rbytes);
+    const int npc = (cend - cbeg + PCS - 1) / PCS;           // pieces per block
     const int nrows = (int)(v1 - v0);
-    const int nst = (nrows + S - 1) / S;
+    const int nrb = (nrows + RL - 1) / RL;
+    const int my_blocks = (warp < nrb) ? (nrb - warp + NW - 1) / NW : 0;
+    const int my_stages = my_blocks * npc;
+    const uint32_t slot0 = smem_u32(smem) + (uint32_t)(warp * D * stage_bytes);
+    const uint32_t wbar = bar0 + 8 * warp * D;
+    const uint32_t xbar = bar0 + 8 * NW * D;
+    // units (blocks, or chunks of bf16) of a row: the last tile may be partial
+    const int units = (WF == W_BF16) ? p.nc : p.nb;
+
+    // stage t of this warp: block warp + NW * (t / npc), piece t % npc
+    auto issue = [&](int t, int slot) {
+        const int bl = t / npc, pc = t - (t / npc) * npc;
+        const int ca = cbeg + pc * PCS;
+        int64_t poff, pbytes;
+        chunk_range_bytes<WF>(ca, min(cend, ca + PCS), poff, pbytes);
+        issue_stage<WF>(p, slot0 + slot * stage_bytes, wbar + 8 * slot, v0 + (int64_t)(warp + NW * bl) * RL, RL, v1,
+                        poff, pbytes);
+    };
 
     if (tid == 0) {
-        for (int i = 0; i < NS; i++) {
-            mbar_init(bar0 + 8 * i, 1);                 // full: producer's arrive + bytes
-            mbar_init(bar0 + 8 * (NS + i), p.wg);       // empty: the group's warps
-        }
+        for (int i = 0; i < NW * D; i++) mbar_init(bar0 + 8 * i, 1);   // lane 0's arrive + bytes
+        mbar_init(xbar, 1);
         s_abort = 0;
         mbar_fence_init();
     }
     __syncthreads();
 
-    if (tid >= ncons) {
-        if (lane == 0) produce_stages<WF>(p, smem, bar0, v0, v1, roff, rbytes, nst, &s_abort);
-        return;
-    }
+    // the warp's first stages, requested before the previous grid completes
+    int issued = 0;
+    const int first = min(D, my_stages);
+    const int early = min(first, p.early);
+    if (lane == 0)
+        for (; issued < early; issued++) issue(issued, issued);
 
     pdl_wait();
     pdl_launch_dependents();
-    stage_x<WF, XF>(p, xs, M, tid, ncons);
-    named_barrier(1, ncons);
+    // The activation rows come in one bulk copy, requested before the rest of
+    // the weight stream so that they do not queue behind it.  The copy covers
+    // the 16-byte-aligned span around X (at most 15 bytes either side, which
+    // never crosses a page), as bulk copies need 16-byte alignment.
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(p.X);
+    const int xoff = (int)(xa & 15);
+    const uint32_t xcopy = (uint32_t)((xoff + M * x_src_row_bytes<XF>(p) + 15) & ~15ll);
+    if (tid == 0) {
+        mbar_arrive_expect_tx(xbar, xcopy);
+        bulk_g2s(smem_u32(smem + p.xraw_off), reinterpret_cast<const void *>(xa - xoff), xcopy, xbar);
+    }
+    __syncthreads();
+    if (lane == 0)
+        for (; issued < first; issued++) issue(issued, issued);
+    const bool xok = mbar_wait_bounded(xbar, 0);
+    if (!xok) {
+        atomicExch(&g_gemv_error, 1);
+        s_abort = 1;
+    }
+    expand_x<WF, XF>(p, smem + p.xraw_off + xoff, xs, M, tid, blockDim.x);
+    __syncthreads();
 
-    const int L = p.L;
-    const int lgL = 31 - __clz(L);
-    const int R = 32 >> lgL;                       // rows per warp per stage
-    const int q = lane >> lgL;                     // which of the warp's rows
-    const int sub = lane & (L - 1);                // lane within the row
-    const int runs = (p.nc + 31) / 32;
+    const int ds_off = ((p.nc + 31) / 32) * XPieces<WF, XF>::P * 512;   // q8_1 (d, sum) table
     const bool swiglu = (p.epi == EPI_SWIGLU);
-    const int grp = warp / p.wg;
-    const int wig = warp - grp * p.wg;
-    const int pr = wig * R + q;                    // row slot within a stage
-    const int r = swiglu ? ((pr >> 1) + ((pr & 1) ? (S >> 1) : 0)) : pr;
-    const int c0 = cbeg + sub;
-    const int J = (c0 < cend) ? (cend - c0 + L - 1) >> lgL : 0;
-    const uint8_t *xm = xs;
+    const int x_row_bytes = p.x_row_bytes;
 
-    int s = grp % NS;
-    uint32_t ph = (uint32_t)((grp / NS) & 1);
-    bool ok = true;
-    for (int j = grp; j < nst; j += p.ng) {
-        if (ok && !mbar_wait_bounded(bar0 + 8 * s, ph)) {
-            atomicExch(&g_gemv_error, 1);
-            s_abort = 1;
+    int d = 0;                                     // slot of the warp's next stage
+    uint32_t ph = 0;
+    int waited = 0;                                // stages whose bytes lane 0 has seen land
+    bool ok = !*(volatile int *)&s_abort;
+    float acc[RL][M][2];
+#pragma unroll
+    for (int i = 0; i < RL; i++)
+#pragma unroll
+        for (int m = 0; m < M; m++) acc[i][m][0] = acc[i][m][1] = 0.f;
+    int bl = 0, pc = 0;                            // block (of this warp) and piece of stage t
+    for (int t = 0; t < my_stages; t++) {
+        if (ok) {
+            if (mbar_wait_bounded(wbar + 8 * d, ph)) {
+                waited++;
+            } else {
+                atomicExch(&g_gemv_error, 1);
+                s_abort = 1;
+            }
         }
         ok = ok && !*(volatile int *)&s_abort;
-        const int64_t vs = v0 + (int64_t)j * S;
-        const int64_t v = staged_vrow(p, vs, S, r);
-        const bool rv = ok && v < v1;
-        const uint8_t *srow = smem + s * stage_bytes + r * p.row_stride;
+        if (ok) {
+            const int ca = cbeg + pc * PCS;
+            const int cb = min(cend, ca + PCS);
+            const int tg = ca / CPT;                                 // first tile (global) of the piece
+            const int nt = (cb - ca + CPT - 1) / CPT;
+            const int tail = min(32, units - 32 * (tg + nt - 1));   // units in the piece's last tile
+            lpr_tiles<WF, XF, M, RL>(acc, smem + (warp * D + d) * stage_bytes, row_stride, xs, x_row_bytes, ds_off, tg,
+                                     nt, tail, lane);
+        }
+        // the warp is done with this slot: refill it with the warp's stage t + D
+        __syncwarp();
+        if (lane == 0 && ok && t + D < my_stages) {
+            fence_proxy_async_smem();
+            issue(t + D, d);
+            issued++;
+        }
+        if (++d == D) { d = 0; ph ^= 1; }
+        if (++pc < npc) continue;
 
-        float acc[M];
+        // the block's last piece: finish its outputs over the warp (fixed butterfly order)
+        pc = 0;
+        const int64_t vb = v0 + (int64_t)(warp + NW * bl) * RL;
+        bl++;
+        float tot[RL][M];
 #pragma unroll
-        for (int m = 0; m < M; m++) acc[m] = 0.f;
-        if (rv) {
-#pragma unroll 4
-            for (int jj = 0; jj < J; jj++) {
-                const int c = c0 + (jj << lgL);
-                if (WF == W_Q8_0 && !chunk_valid<WF>(c, p.nb, p.nc)) continue;
-                WChunk<WF> wc;
-                lds_w<WF>(wc, srow, roff, c);
+        for (int i = 0; i < RL; i++)
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                float a = acc[i][m][0] + acc[i][m][1];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+                tot[i][m] = a;
+                acc[i][m][0] = acc[i][m][1] = 0.f;
+            }
+        if (lane != 0 || !ok) continue;
+        if (swiglu) {
+            // rows 0 .. RL/2-1 are gates, RL/2 .. RL-1 the matching ups
+#pragma unroll
+            for (int k = 0; k < RL / 2; k++) {
+                const int64_t v = staged_vrow(p, vb, RL, k);
+                if (v >= v1) continue;
+#pragma unroll
+                for (int m = 0; m < M; m++)
+                    p.Y[0][(int64_t)m * p.rows[0] + (v >> 1)] = silu(tot[k][m]) * tot[RL / 2 + k][m];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < RL; i++) {
+                const int64_t v = staged_vrow(p, vb, RL, i);
+                if (v >= v1) continue;
 #pragma unroll
                 for (int m = 0; m < M; m++) {
-                    XSlice<WF, XF> x;
-                    lds_x<WF, XF>(x, xm + m * p.x_row_bytes, c, runs);
-                    acc[m] += chunk_dot<WF, XF>(wc, x);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar0 + 8 * (NS + s));       // this warp is done with stage s
-        s += p.ng;
-        while (s >= NS) { s -= NS; ph ^= 1; }
-
-        // finish the row over its L lanes (fixed butterfly order)
-#pragma unroll
-        for (int m = 0; m < M; m++)
-            for (int off = L >> 1; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
-        if (swiglu) {
-            // lane groups 2i (gate) and 2i+1 (up) hold one output
-#pragma unroll
-            for (int m = 0; m < M; m++) {
-                const float u = __shfl_down_sync(0xffffffffu, acc[m], L);
-                if (rv && sub == 0 && (q & 1) == 0)
-                    p.Y[0][(int64_t)m * p.rows[0] + (v >> 1)] = silu(acc[m]) * u;
-            }
-        } else if (rv && sub == 0) {
-#pragma unroll
-            for (int m = 0; m < M; m++) {
-                if (p.epi == EPI_PARTIAL) {
-                    p.ws[((int64_t)split * M + m) * p.Nv + v] = acc[m];
-                } else {
-                    int mat; int64_t rr;
-                    map_row(p, v, mat, rr);
-                    p.Y[mat][(int64_t)m * p.rows[mat] + rr] = acc[m];
+                    if (p.epi == EPI_PARTIAL) {
+                        p.ws[((int64_t)split * M + m) * p.Nv + v] = tot[i][m];
+                    } else {
+                        int mat; int64_t rr;
+                        map_row(p, v, mat, rr);
+                        p.Y[mat][(int64_t)m * p.rows[mat] + rr] = tot[i][m];
+                    }
                 }
             }
         }
     }
+    // after a timeout: do not leave while this CTA's copies are in flight
+    if (lane == 0) {
+        for (int t = waited; t < issued; t++)
+            mbar_wait_bounded(wbar + 8 * (t % D), (uint32_t)((t / D) & 1));
+    }
+    if (tid == 0 && !xok) mbar_wait_bounded(xbar, 0);
 }
 
-template <int WF, int XF, int M, bool COMPACT>
+template <int WF, int XF, int M, int RL>
 __host__ cudaError_t gemv_lpr_launch_one(const GemvParams &p, dim3 grid, int threads, size_t smem,
                                          cudaStream_t stream, bool pdl, int *occupancy)
 {
-    auto kern = gemv_lpr_kernel<WF, XF, M, COMPACT>;
+    auto kern = gemv_lpr_kernel<WF, XF, M, RL>;
     if (occupancy) {
         int dev = 0, optin = 0;
         cudaFuncAttributes fa;
@@ -838,14 +1134,16 @@ __host__ cudaError_t gemv_lpr_launch_one(const GemvParams &p, dim3 grid, int thr
 }
 
 template <int WF, int XF>
-__host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, bool compact, dim3 grid, int threads, size_t smem,
+__host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, int threads, size_t smem,
                                        cudaStream_t stream, bool pdl, int *occupancy)
 {
     constexpr int XR = (XF == X_BF16) ? X_F32 : XF;      // staged bf16 activations are fp32
-    if (M == 1 && compact) return gemv_lpr_launch_one<WF, XR, 1, true>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 1) return gemv_lpr_launch_one<WF, XR, 1, false>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 2 && compact) return gemv_lpr_launch_one<WF, XR, 2, true>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 2) return gemv_lpr_launch_one<WF, XR, 2, false>(p, grid, threads, smem, stream, pdl, occupancy);
+    const int rl = p.rl;
+    if (M == 1 && rl == 1) return gemv_lpr_launch_one<WF, XR, 1, 1>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 1 && rl == 2) return gemv_lpr_launch_one<WF, XR, 1, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 1 && rl == 4) return gemv_lpr_launch_one<WF, XR, 1, 4>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 2 && rl == 1) return gemv_lpr_launch_one<WF, XR, 2, 1>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 2 && rl == 2) return gemv_lpr_launch_one<WF, XR, 2, 2>(p, grid, threads, smem, stream, pdl, occupancy);
     return cudaErrorInvalidValue;
 }
 

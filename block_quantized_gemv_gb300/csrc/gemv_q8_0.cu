@@ -8,10 +8,10 @@ cudaError_t gemv_run_q8_0(const GemvParams &p, int M, int C, dim3 grid, int thre
     return gemv_dispatch<W_Q8_0, X_BF16>(p, M, C, grid, threads, smem, stream, pdl, occupancy);
 }
 cudaError_t gemv_error_q8_0(int *out) { return gemv_take_error(out); }
-cudaError_t gemv_lpr_run_q8_0(const GemvParams &p, int M, bool compact, dim3 grid, int threads, size_t smem, cudaStream_t stream,
+cudaError_t gemv_lpr_run_q8_0(const GemvParams &p, int M, dim3 grid, int threads, size_t smem, cudaStream_t stream,
                             bool pdl, int *occupancy)
 {
-    return gemv_lpr_dispatch<W_Q8_0, X_BF16>(p, M, compact, grid, threads, smem, stream, pdl, occupancy);
+    return gemv_lpr_dispatch<W_Q8_0, X_BF16>(p, M, grid, threads, smem, stream, pdl, occupancy);
 }
 int gemv_x_stage_bytes_q8_0(int nc, int nb) { return x_stage_row_bytes<W_Q8_0, X_F32>(nc, nb); }
 }  // namespace bqg

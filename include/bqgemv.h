@@ -199,7 +199,7 @@ size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K);
 int bqg_last_device_error(cudaStream_t stream, int *out);
 
 /* Programmatic dependent launch for the GEMV kernels (default off).
- * When on, a GEMV may start and prefetch its weights into L2 while the
+ * When on, a GEMV may start and begin streaming its weights while the
  * previous kernel on the stream finishes; it waits for that kernel before
  * reading X or writing Y.  Weights must not be written by a kernel that is
  * still running when the GEMV is enqueued.  Returns the previous setting. */
