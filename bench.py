@@ -72,6 +72,23 @@ def profiled_traffic(kernel_key):
     return e.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(value, dist, device="cuda"):
+    """The largest `value` over all ranks (every rank receives it); `value`
+    itself on a single process.  The timed region of a replica run is the
+    slowest rank's."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_call, calls_per_rank, world, seconds):
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return bytes_per_call * calls_per_rank * world / seconds / 1e9
+
+
 def divisor_repeats(K, cap=10):
     for r in range(min(cap, K), 0, -1):
         if K % r == 0:
@@ -358,12 +375,7 @@ def time_arm(arm, steps, warmup, use_graph=True, min_warm_s=1.0, sampler=None, d
     if sampler:
         sampler.stop()
     times = [a.elapsed_time(b) / 1e3 for a, b in ev]     # seconds per repeat
-    total = sum(times)
-    if dist is not None:
-        import torch.distributed as tdist
-        t = torch.tensor([total], device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total = float(t.item())
+    total = max_over_ranks(sum(times), dist)
     mean = statistics.mean(times)
     spread = (max(times) - min(times)) / mean if mean > 0 else 0.0
     return {"seconds": total, "per_repeat_s": times, "repeats": repeats, "launches_per_repeat": L,
@@ -534,7 +546,7 @@ def main():
         t = t2
     rec = arm_record(head, t, peaks)
     calls = args.steps
-    value = gb_s(head.bytes_per_call * calls * world, t["seconds"])
+    value = whole_job_gbs(head.bytes_per_call, calls, world, t["seconds"])
     clocks = sampler.summary()
 
     e2e_s = time_e2e(head, args.steps)

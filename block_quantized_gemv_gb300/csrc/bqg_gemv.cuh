@@ -624,38 +624,6 @@ __host__ __device__ __forceinline__ int x_stage_row_bytes(int nc, int nb)
     return runs * XPieces<WF, XF>::P * 512 + ((XF == X_Q8_1) ? nb * 8 : 0);
 }
 
-template <int WF, int XF>
-__device__ __forceinline__ void stage_x(const GemvParams &p, uint8_t *xs, int M, int tid, int nthr)
-{
-    constexpr int P = XPieces<WF, XF>::P;
-    const int runs = (p.nc + 31) / 32;
-    for (int m = 0; m < M; m++) {
-        uint8_t *xr = xs + (size_t)m * p.x_row_bytes;
-        for (int i = tid; i < p.nc * P; i += nthr) {
-            const int c = i / P, pc = i - (i / P) * P;
-            if (!chunk_valid<WF>(c, p.nb, p.nc)) continue;
-            uint4 v;
-            if constexpr (XF == X_Q8_1) {
-                const uint32_t *blk = reinterpret_cast<const uint32_t *>(p.X + ((int64_t)m * p.nb + c) * Q8_1_BYTES);
-                v = make_uint4(__ldg(blk + 1 + 4 * pc), __ldg(blk + 2 + 4 * pc), __ldg(blk + 3 + 4 * pc),
-                               __ldg(blk + 4 + 4 * pc));
-                if (pc == 0) {
-                    int sum = 0;
-                    for (int k = 0; k < 8; k++) sum = __dp4a((int)__ldg(blk + 1 + k), 0x01010101, sum);
-                    float2 ds = make_float2(half_bits_to_float(__ldg(blk) & 0xffffu), __int_as_float(sum));
-                    *reinterpret_cast<float2 *>(xr + (size_t)runs * P * 512 + (size_t)c * 8) = ds;
-                }
-            } else {
-                // four consecutive bf16 -> fp32
-                const uint2 w = __ldg(reinterpret_cast<const uint2 *>(
-                    p.X + ((int64_t)m * p.K + chunk_elem0<WF>(c) + 4 * pc) * 2));
-                v = make_uint4(w.x << 16, w.x & 0xffff0000u, w.y << 16, w.y & 0xffff0000u);
-            }
-            *reinterpret_cast<uint4 *>(xr + ((size_t)(c >> 5) * P + pc) * 512 + (c & 31) * 16) = v;
-        }
-    }
-}
-
 // Bytes of one activation row as the caller passes it: q8_1 blocks, or bf16
 // (staged as fp32).
 template <int XF>
@@ -664,8 +632,9 @@ __device__ __forceinline__ int64_t x_src_row_bytes(const GemvParams &p)
     return (XF == X_Q8_1) ? (int64_t)p.nb * Q8_1_BYTES : (int64_t)p.K * 2;
 }
 
-// The same staged layout as stage_x, built from a raw copy of the M
-// activation rows in shared memory (`raw` points at X[0]).
+// Build the staged layout from a raw copy of the M activation rows in
+// shared memory (`raw` points at X[0]): bf16 become fp32; q8_1 blocks give
+// their codes and a (d, exact sum of codes) pair.
 template <int WF, int XF>
 __device__ __forceinline__ void expand_x(const GemvParams &p, const uint8_t *raw, uint8_t *xs, int M, int tid, int nthr)
 {
