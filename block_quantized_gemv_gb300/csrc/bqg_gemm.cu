@@ -1,22 +1,31 @@
 // bqg_gemm.cu -- prefill GEMM Y[M x N] = X[M x K] W^T on the sm_103a tensor cores.
 //
 // The tiled prefill GEMM of "llama-3x-prompt-speed" ("the tile"): a weight
-// tile is unpacked once into shared memory and serves every activation row
-// of the tile, instead of being unpacked once per row.  Here the unit of
-// work is 128 weight rows x 128 activation rows; per k-step of 64:
+// tile is unpacked once and serves every activation row of the tile,
+// instead of being unpacked once per row.  Here the unit of work is 128
+// weight rows x 128 activation rows; per k-step of 64:
 //   * warps 1-8 (one q4_0 block of one weight row per thread) load the codes
-//     and scale eight k-steps ahead, dequantize (q - 8) * d exactly in fp32
-//     and round once to bf16, and write the 128 x 64 bf16 tile into shared
-//     memory in the K-major 128-byte-swizzled layout the tensor core reads;
-//   * warp 0, lane 0 loads the matching 128 x 64 bf16 activation tile with
-//     one TMA copy (same swizzle) and issues four tcgen05.mma.kind::f16
-//     (M = 128 weight rows, N = 128 activations, K = 16) accumulating fp32
-//     in tensor memory; tcgen05.commit frees the stage;
+//     and scale eight k-steps ahead, dequantize (q - 8) * d exactly in fp32,
+//     round once to bf16 and store the 128 x 64 bf16 tile straight into
+//     tensor memory (tcgen05.st: lane = weight row, two k per column), where
+//     the MMA reads its A operand.  Shared memory then carries only the
+//     activation tiles: with A staged there too, its bandwidth (dequant
+//     writes, TMA writes and both MMA operands, 64 KiB per k-step) bounded
+//     the loop at twice the MMA time;
+//   * warp 13, lane 0 loads the matching 128 x 64 bf16 activation tile with
+//     one TMA copy (same swizzle) as soon as the stage is free;
+//   * warp 0, lane 0 issues four tcgen05.mma.kind::f16 (A from tensor
+//     memory, B from shared memory; M = 128 weight rows, N = 128
+//     activations, K = 16) accumulating fp32 in tensor memory as soon as both
+//     halves of the stage are in place; tcgen05.commit frees the stage.  It
+//     never waits for its own MMAs, so the tensor core always has the next
+//     K-step queued;
 //   * warps 9-12 read the finished 128 x 128 fp32 accumulator with
 //     tcgen05.ld (each warp its 32 lanes = 32 weight rows) and store
 //     Y[m][n] coalesced along n.
-// The accumulator is double-buffered (256 TMEM columns) so the epilogue of
-// one unit overlaps the MMAs of the next.  The kernel is persistent (one
+// Tensor memory (512 columns): two 128-column accumulators, so the epilogue
+// of one unit overlaps the MMAs of the next, then the NSTAGE A slots of 32
+// columns.  The kernel is persistent (one
 // CTA per SM).  Every mbarrier wait is bounded: on a timeout the kernel sets
 // g_gemm_error, stops issuing work, drains what it started and frees TMEM.
 #include <mutex>
@@ -36,14 +45,18 @@ namespace {
 constexpr int TM = 128;         // weight rows per unit (MMA M)
 constexpr int TN = 128;         // activation rows per unit (MMA N)
 constexpr int TK = 64;          // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int NSTAGE = 6;
-constexpr int TILE_BYTES = TM * TK * 2;       // 16 KiB, both operands
-constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+constexpr int NSTAGE = 8;
+constexpr int TILE_BYTES = TN * TK * 2;       // 16 KiB activation tile
+constexpr int STAGE_BYTES = TILE_BYTES;
 constexpr int ACC_COLS = TN;                  // fp32 columns per accumulator
-constexpr int TMEM_COLS = 2 * ACC_COLS;       // double buffer
+constexpr int A_COL0 = 2 * ACC_COLS;          // first column of the A slots
+constexpr int A_COLS = TK / 2;                // 32-bit columns of one A slot (two bf16 each)
+constexpr int TMEM_COLS = 512;                // 2 accumulators + NSTAGE A slots
+static_assert(A_COL0 + NSTAGE * A_COLS <= TMEM_COLS, "tensor memory budget");
 constexpr int DQ_WARPS = 8;                   // dequantizing warps (1..8)
 constexpr int EPI_WARP0 = 1 + DQ_WARPS;       // epilogue warps 9..12
-constexpr int NUM_THREADS = (EPI_WARP0 + 4) * 32;
+constexpr int TMA_WARP = EPI_WARP0 + 4;       // activation loads: warp 13
+constexpr int NUM_THREADS = (TMA_WARP + 1) * 32;
 constexpr int PREFETCH = 8;                   // k-steps of weight codes in flight per thread
 
 // shared memory map (dynamic, 1024-byte aligned)
@@ -71,9 +84,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
-// byte offset of 16-byte chunk c (k = 8c..8c+7) of row r in a K-major
-// 128-byte-swizzled tile
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
 {
@@ -82,13 +92,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
                  : "memory");
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate)
+// D[tmem] (+)= A[tmem] * B[smem descriptor]
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t accumulate)
 {
     asm volatile("{\n\t.reg .pred p;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(IDESC), "r"(accumulate)
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(IDESC), "r"(accumulate)
                  : "memory");
+}
+
+// 32 lanes x 16 columns of 32-bit words into tensor memory (this warp's lane
+// quarter), then wait until they are written
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 ::"r"(taddr), "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y),
+                   "r"(v[1].z), "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x),
+                   "r"(v[3].y), "r"(v[3].z), "r"(v[3].w)
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -199,36 +223,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
     };
 
     if (warp == 0) {
-        // ---------------- TMA issuer + MMA issuer ----------------
+        // ---------------- MMA issuer ----------------
         if (lane == 0) {
             int it = 0;        // global k-step counter across units (ring position)
             int ucount = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ucount++) {
-                const int tn = u % a.tiles_n, tm = u / a.tiles_n;      // weight tile, activation tile
-                (void)tn;
                 const int b = ucount & 1;
                 // the accumulator must have been read out (two units ago)
                 if (ucount >= 2 && !mbar_wait_spin(bar_acce(b), ((ucount >> 1) - 1) & 1)) { fail(); ok = false; break; }
                 tc_fence_after();
                 const uint32_t dacc = tmem + b * ACC_COLS;
-                // keep up to NSTAGE activation tiles in flight ahead of the MMAs
-                int issued = it;
-                auto issue_x = [&](int step) {
-                    const int s = step % NSTAGE;
-                    const int ks = step - it;      // k-step within this unit
-                    if (step >= NSTAGE && !mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1)) return false;
-                    mbar_arrive_expect_tx(bar_fullX(s), TILE_BYTES);
-                    tma_load_2d(sbase + OFF_STAGES + s * STAGE_BYTES + TILE_BYTES, &xmap, ks * TK, tm * TN, bar_fullX(s));
-                    return true;
-                };
                 for (int k = 0; k < nk && ok; k++) {
                     const int step = it + k;
-                    while (issued < it + nk && issued < step + NSTAGE) {
-                        if (!issue_x(issued)) { fail(); ok = false; break; }
-                        issued++;
-                    }
-                    if (!ok) break;
                     const int s = step % NSTAGE;
                     const uint32_t ph = (step / NSTAGE) & 1;
                     if (!mbar_wait_spin(bar_fullX(s), ph) || !mbar_wait_spin(bar_fullW(s), ph)) {
@@ -236,11 +243,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
                     }
                     if (*abort_flag) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t aw = sbase + OFF_STAGES + s * STAGE_BYTES;       // weights: MMA A (M = 128 rows)
-                    const uint32_t bx = aw + TILE_BYTES;                            // activations: MMA B (N = 128)
+                    const uint32_t aw = tmem + A_COL0 + s * A_COLS;                 // weights: MMA A (M = 128 rows)
+                    const uint32_t bx = sbase + OFF_STAGES + s * STAGE_BYTES;       // activations: MMA B (N = 128)
 #pragma unroll
                     for (int kk = 0; kk < TK / 16; kk++)
-                        umma_bf16(dacc, sw128_desc(aw + kk * 32), sw128_desc(bx + kk * 32), (k > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts(dacc, aw + kk * 8, sw128_desc(bx + kk * 32), (k > 0 || kk > 0) ? 1u : 0u);
                     umma_commit(bar_empty(s));               // stage s is free when these MMAs finish
                 }
                 if (ok) umma_commit(bar_accf(b));            // the unit's accumulator is complete
@@ -250,11 +257,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
             if (it > 0) mbar_wait_spin(bar_empty((it - 1) % NSTAGE), ((it - 1) / NSTAGE) & 1);
         }
         __syncwarp();
+    } else if (warp == TMA_WARP) {
+        // ---------------- activation tiles (TMA) ----------------
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                const int tm = u / a.tiles_n;                      // activation tile
+                for (int k = 0; k < nk; k++) {
+                    const int step = it + k;
+                    const int s = step % NSTAGE;
+                    if (step >= NSTAGE && !mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1)) {
+                        fail(); ok = false; break;
+                    }
+                    if (*abort_flag) { ok = false; break; }
+                    mbar_arrive_expect_tx(bar_fullX(s), TILE_BYTES);
+                    tma_load_2d(sbase + OFF_STAGES + s * STAGE_BYTES, &xmap, k * TK, tm * TN, bar_fullX(s));
+                }
+                it += nk;
+            }
+        }
+        __syncwarp();
     } else if (warp <= DQ_WARPS) {
         // ---------------- weight dequantization (warps 1-8) ----------------
-        const int t = threadIdx.x - 32;
-        const int r = t & (TM - 1);                          // weight row in the unit
-        const int h = t >> 7;                                // which of the step's two blocks
+        // a warp may only reach its lane quarter of tensor memory: warps 1-4 and
+        // 5-8 each cover quarters 1, 2, 3, 0, for the step's first and second block
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;                   // weight row in the unit
+        const int h = (warp - 1) >> 2;                       // which of the step's two blocks
+        const uint32_t arow = tmem + ((uint32_t)(quarter * 32) << 16) + A_COL0 + h * (A_COLS / 2);
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
@@ -286,20 +317,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
                     if (k >= nk) break;
                     const int step = it + k;
                     const int s = step % NSTAGE;
-                    if (step >= NSTAGE && !mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1)) {
-                        fail(); ok = false; break;
-                    }
+                    // the whole warp takes the same branch (tcgen05.st is warp-wide)
+                    const bool free_slot = step < NSTAGE || mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1);
+                    if (!__all_sync(0xffffffffu, free_slot)) { fail(); ok = false; break; }
                     if (*abort_flag) { ok = false; break; }
                     const uint4 c0 = cr[i];
                     const float d = half_bits_to_float(sr[i]);
                     load(k + PREFETCH, cr[i], sr[i]);
-                    uint8_t *wt = smem + OFF_STAGES + s * STAGE_BYTES;
-                    // block h covers k 32h .. 32h+31 of the step: chunks 4h .. 4h+3
-                    *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 0)) = dequant8(c0.x, c0.y, 0, d);
-                    *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 1)) = dequant8(c0.z, c0.w, 0, d);
-                    *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 2)) = dequant8(c0.x, c0.y, 4, d);
-                    *reinterpret_cast<uint4 *>(wt + sw128_off(r, 4 * h + 3)) = dequant8(c0.z, c0.w, 4, d);
-                    fence_proxy_async_smem();                      // generic-proxy writes -> tensor core reads
+                    // block h covers k 32h .. 32h+31 of the step: 16 columns of the slot
+                    const uint4 v[4] = {dequant8(c0.x, c0.y, 0, d), dequant8(c0.z, c0.w, 0, d),
+                                        dequant8(c0.x, c0.y, 4, d), dequant8(c0.z, c0.w, 4, d)};
+                    tmem_st16(arow + s * A_COLS, v);
+                    tc_fence_before();                             // tensor-memory writes -> the MMA thread
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_fullW(s));
                 }
