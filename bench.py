@@ -267,16 +267,20 @@ class GemmArm(Arm):
 
 
 class DecodeLayerArm(Arm):
-    """q4_0 x q8_1 decode layer: quantize(x), QKV, gate+up+SwiGLU, quantize(h), down."""
+    """q4_0 x q8_1 decode layer: quantize(x), QKV, gate+up+SwiGLU, quantize(h), down.
+    With fused_norm the layer starts from the raw activation row and its first
+    step is the fused RMSNorm -> q8_1 encoder instead of a plain encoder."""
 
-    def __init__(self, seed=5, K=4096, Nq=4096, Nff=11008):
+    def __init__(self, seed=5, K=4096, Nq=4096, Nff=11008, fused_norm=False):
         import torch
         import block_quantized_gemv_gb300 as bqg
         from block_quantized_gemv_gb300 import synth
         super().__init__()
         self.bqg, self.torch = bqg, torch
-        self.name = f"q4_0 x q8_1 decode layer M=1 (QKV 3x{Nq}x{K}, gate+up 2x{Nff}x{K}, down {K}x{Nff})"
-        self.kernel_key = "decode_layer_q4_0_q8_1"
+        self.fused_norm = fused_norm
+        self.name = (f"q4_0 x q8_1 decode layer M=1 (QKV 3x{Nq}x{K}, gate+up 2x{Nff}x{K}, down {K}x{Nff})"
+                     + (", fused RMSNorm->q8_1" if fused_norm else ""))
+        self.kernel_key = "decode_layer_q4_0_q8_1" + ("_fused_norm" if fused_norm else "")
         self.launches_per_call = 5
         self.K, self.Nq, self.Nff = K, Nq, Nff
 
@@ -287,7 +291,8 @@ class DecodeLayerArm(Arm):
         base = {"Wq": mk(Nq, K, seed), "Wk": mk(Nq, K, seed + 1), "Wv": mk(Nq, K, seed + 2),
                 "Wg": mk(Nff, K, seed + 3), "Wu": mk(Nff, K, seed + 4), "Wd": mk(K, Nff, seed + 5)}
         w_bytes = sum(v.numel() for v in base.values())
-        x = torch.from_numpy(synth.rms_normalised_f32(1, K, seed + 6)).cuda().to(torch.bfloat16)
+        x = torch.from_numpy(synth.activations_f32(1, K, seed + 6) if fused_norm else
+                             synth.rms_normalised_f32(1, K, seed + 6)).cuda().to(torch.bfloat16)
         self.bytes_per_call = (w_bytes + K * 2 + (K // 32) * 36 * 2 + 3 * Nq * 4 + Nff * 4 * 2 +
                                (Nff // 32) * 36 * 2 + K * 4)
         self.R = self.rotation(self.bytes_per_call)
@@ -307,7 +312,10 @@ class DecodeLayerArm(Arm):
 
     def call(self, i):
         b, s = self.bqg, self.sets[i % self.R]
-        b.quantize_q8_1(s["x"], out=s["xq"])
+        if self.fused_norm:
+            b.rmsnorm_quantize_q8_1(s["x"], None, 1e-5, out=s["xq"])
+        else:
+            b.quantize_q8_1(s["x"], out=s["xq"])
         b.gemv_q4_0_q8_1_qkv(s["Wq"], s["Wk"], s["Wv"], s["xq"], self.Nq, self.Nq, self.K,
                              out=(s["q"], s["k"], s["v"]), ws=s["ws_qkv"])
         b.gemv_q4_0_q8_1_gate_up_swiglu(s["Wg"], s["Wu"], s["xq"], self.Nff, self.K, out=s["h"], ws=s["ws_gu"])
@@ -559,7 +567,7 @@ def main():
     other = [GemvArm(bqg.Q8_0, bqg.BF16, 1, N_HEAD, K_HEAD), GemvArm(bqg.Q4_0, bqg.Q8_1, 1, N_HEAD, K_HEAD),
              GemmArm()]
     if args.suite == "full":
-        other += [GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096), DecodeLayerArm()]
+        other += [GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096), DecodeLayerArm(), DecodeLayerArm(fused_norm=True)]
         for M in (1, 2, 4, 8):
             for f in (bqg.BF16, bqg.Q8_0, bqg.Q4_0):
                 other.append(GemvArm(f, bqg.BF16, M, 14336, 4096))

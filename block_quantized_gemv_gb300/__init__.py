@@ -30,6 +30,7 @@ EXPORTS = {
     "bqg_quantize_weights": (["i", "p", "p", "i64", "i64", "p"], "i"),
     "bqg_repack_weights": (["i", "p", "p", "i64", "i64", "p"], "i"),
     "bqg_quantize_q8_1": (["p", "i", "p", "i", "i64", "p"], "i"),
+    "bqg_rmsnorm_quantize_q8_1": (["p", "i", "p", "f", "p", "i", "i64", "p"], "i"),
     "bqg_gemv_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemv_q8_0": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemv_q4_0": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
@@ -48,7 +49,7 @@ EXPORTS = {
     "bqg_noalloc_scratch_bytes": ([], "size"),
 }
 _CT = {"i": ctypes.c_int, "i64": ctypes.c_int64, "p": ctypes.c_void_p, "size": ctypes.c_size_t,
-       "str": ctypes.c_char_p}
+       "str": ctypes.c_char_p, "f": ctypes.c_float}
 
 _lock = threading.Lock()
 _lib = None
@@ -159,6 +160,23 @@ def quantize_q8_1(x: torch.Tensor, out: torch.Tensor | None = None, stream=None)
         out = torch.empty((M, row_bytes(Q8_1, K)), dtype=torch.uint8, device=x.device)
     _check(load().bqg_quantize_q8_1(_dev(x, "x"), dt, _dev(out, "out", numel=M * row_bytes(Q8_1, K)), M, K,
                                     _stream(stream)), "bqg_quantize_q8_1")
+    return out
+
+
+def rmsnorm_quantize_q8_1(x: torch.Tensor, gamma: torch.Tensor | None = None, eps: float = 1e-5,
+                          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Fused RMSNorm (optional fp32 gain `gamma`) + q8_1 quantization:
+    bf16 or fp32 M x K -> q8_1 blocks (uint8, M x K/32*36)."""
+    M, K = x.shape
+    dt = {torch.bfloat16: BF16, torch.float32: F32}.get(x.dtype)
+    if dt is None:
+        raise TypeError("x must be bf16 or fp32")
+    if out is None:
+        out = torch.empty((M, row_bytes(Q8_1, K)), dtype=torch.uint8, device=x.device)
+    g = None if gamma is None else _dev(gamma, "gamma", torch.float32, K * 4)
+    _check(load().bqg_rmsnorm_quantize_q8_1(_dev(x, "x"), dt, g, float(eps),
+                                            _dev(out, "out", numel=M * row_bytes(Q8_1, K)), M, K, _stream(stream)),
+           "bqg_rmsnorm_quantize_q8_1")
     return out
 
 

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <map>
+#include <cmath>
 #include <mutex>
 #include <tuple>
 
@@ -28,6 +29,7 @@ int gemv_x_stage_bytes_q8_0(int, int);
 int gemv_x_stage_bytes_q4_0(int, int);
 int gemv_x_stage_bytes_q4_0_q8_1(int, int);
 cudaError_t launch_quantize_q8_1(const void *, int, void *, int, int64_t, cudaStream_t, bool);
+cudaError_t launch_rmsnorm_q8_1(const void *, int, const float *, float, void *, int, int64_t, cudaStream_t, bool);
 cudaError_t launch_quantize_weights(int, const float *, void *, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_repack(int, const void *, void *, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_block_dots(const void *, const void *, int32_t *, int64_t, int64_t, int64_t, cudaStream_t);
@@ -522,6 +524,19 @@ int bqg_quantize_q8_1(const void *x, int x_dtype, void *xq, int M, int64_t K, cu
     DevInfo dev;
     if (int st = current_device(&dev)) return st;
     return cuda_status(launch_quantize_q8_1(x, x_dtype == BQG_F32, xq, M, K, stream, g_pdl.load() != 0));
+}
+
+int bqg_rmsnorm_quantize_q8_1(const void *x, int x_dtype, const float *gamma, float eps, void *xq, int M, int64_t K,
+                              cudaStream_t stream)
+{
+    if (!x || !xq || M < 1 || M > 65535 || (x_dtype != BQG_BF16 && x_dtype != BQG_F32)) return BQG_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (!aligned(x, x_dtype == BQG_F32 ? 4 : 2) || !aligned(xq, 4) || (gamma && !aligned(gamma, 4)))
+        return BQG_ERR_MISALIGNED;
+    DevInfo dev;
+    if (int st = current_device(&dev)) return st;
+    return cuda_status(launch_rmsnorm_q8_1(x, x_dtype == BQG_F32, gamma, eps, xq, M, K, stream, g_pdl.load() != 0));
 }
 
 int bqg_gemv_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws, size_t ws_bytes,

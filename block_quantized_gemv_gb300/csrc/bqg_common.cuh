@@ -136,6 +136,49 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity)
 // async-proxy ones (bulk copies, tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// ---------------------------------------------------------------------------
+// q8 block encoding (one warp per 32-element block, lane i = element i):
+// d = fp16_rn(amax / 127), q = round_half_away(x / d) in IEEE fp32, clamped
+// to [-127, 127]; d == 0 gives q = 0.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_sum_int(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+// q8 code of v given the stored scale d (as float)
+__device__ __forceinline__ int q8_code(float v, float d)
+{
+    if (d == 0.0f) return 0;
+    const float q = fminf(fmaxf(roundf(__fdiv_rn(v, d)), -127.0f), 127.0f);
+    return (int)q;
+}
+
+// One q8_1 block (36 bytes at `out`, 4-byte aligned): fp16 d, fp16 s =
+// fp16_rn(d * sum q), 32 int8 codes; `v` is this lane's element.
+__device__ __forceinline__ void q8_1_encode_warp(float v, int lane, uint8_t *out)
+{
+    const float amax = warp_max(fabsf(v));
+    const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    const float d = __half2float(dh);
+    const int q = q8_code(v, d);
+    const int sum = warp_sum_int(q);
+    out[4 + lane] = (uint8_t)(int8_t)q;
+    if (lane == 0) {
+        // d | s as one little-endian word
+        const __half sh = __float2half_rn(d * (float)sum);   // exact product, one rounding
+        const uint32_t db = __half_as_ushort(dh), sb = __half_as_ushort(sh);
+        *reinterpret_cast<uint32_t *>(out) = db | (sb << 16);
+    }
+}
+
 // Bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)

@@ -15,18 +15,6 @@
 
 namespace bqg {
 
-__device__ __forceinline__ float warp_max(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ int warp_sum_int(int v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 __device__ __forceinline__ float load_act(const void *x, int x_f32, int64_t i)
 {
@@ -35,13 +23,6 @@ __device__ __forceinline__ float load_act(const void *x, int x_f32, int64_t i)
     return __uint_as_float((uint32_t)b << 16);
 }
 
-// q8 code of v given the stored scale d (as float)
-__device__ __forceinline__ int q8_code(float v, float d)
-{
-    if (d == 0.0f) return 0;
-    const float q = fminf(fmaxf(roundf(__fdiv_rn(v, d)), -127.0f), 127.0f);
-    return (int)q;
-}
 
 // M x K activations -> M x K/32 q8_1 blocks (36 B)
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restrict__ x, int x_f32,
@@ -54,19 +35,47 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
     const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (blk >= nblocks) return;
     const int64_t m = blk / nb, b = blk - (blk / nb) * nb;
-    const float v = load_act(x, x_f32, m * K + b * QK + lane);
-    const float amax = warp_max(fabsf(v));
-    const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
-    const float d = __half2float(dh);
-    const int q = q8_code(v, d);
-    const int sum = warp_sum_int(q);
-    uint8_t *out = xq + blk * Q8_1_BYTES;
-    out[4 + lane] = (uint8_t)(int8_t)q;
-    if (lane == 0) {
-        // d | s as one little-endian word (blocks are 4-byte aligned)
-        const __half sh = __float2half_rn(d * (float)sum);   // exact product, one rounding
-        const uint32_t db = __half_as_ushort(dh), sb = __half_as_ushort(sh);
-        *reinterpret_cast<uint32_t *>(out) = db | (sb << 16);
+    q8_1_encode_warp(load_act(x, x_f32, m * K + b * QK + lane), lane, xq + blk * Q8_1_BYTES);
+}
+
+// Fused RMSNorm -> q8_1, one CTA per activation row ("MI50 megakernel",
+// hypothesis ledger: neighbouring steps fused into one dispatch; the Q8_1
+// activation of "rx-6700xt-llama2-decode").  s = sum x^2 is accumulated in
+// fp64, which is exact for bf16 inputs whatever the order (each square has
+// 16 significant bits), r = fp32(1 / sqrt(s / K + eps)) in fp64, then
+// y = fp32(fp32(x * r) * gamma) goes through the q8_1 encoder, one warp per
+// block.
+__global__ void __launch_bounds__(256) rmsnorm_q8_1_kernel(const void *__restrict__ x, int x_f32,
+                                                           const float *__restrict__ gamma, float eps,
+                                                           uint8_t *__restrict__ xq, int nb, int64_t K)
+{
+    __shared__ double part[8];
+    __shared__ float s_r;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t m = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    double s = 0.0;
+    for (int64_t k = tid; k < K; k += 256) {
+        const double v = (double)load_act(x, x_f32, m * K + k);
+        s += v * v;                                   // exact square (<= 48 bits)
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) part[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+        double t = 0.0;
+        for (int w = 0; w < 8; w++) t += part[w];
+        s_r = (float)(1.0 / sqrt(t / (double)K + (double)eps));
+    }
+    __syncthreads();
+    const float r = s_r;
+    for (int b = warp; b < nb; b += 8) {
+        const int64_t k = (int64_t)b * QK + lane;
+        float y = __fmul_rn(load_act(x, x_f32, m * K + k), r);
+        if (gamma) y = __fmul_rn(y, gamma[k]);
+        q8_1_encode_warp(y, lane, xq + (m * nb + b) * Q8_1_BYTES);
     }
 }
 
@@ -190,6 +199,21 @@ cudaError_t launch_quantize_q8_1(const void *x, int x_f32, void *xq, int M, int6
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel, x, x_f32, (uint8_t *)xq, nblocks, nb, K);
+}
+
+cudaError_t launch_rmsnorm_q8_1(const void *x, int x_f32, const float *gamma, float eps, void *xq, int M, int64_t K,
+                               cudaStream_t s, bool pdl)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)M);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, rmsnorm_q8_1_kernel, x, x_f32, gamma, eps, (uint8_t *)xq, (int)(K / QK), K);
 }
 
 cudaError_t launch_quantize_weights(int fmt, const float *W, void *dst, int64_t N, int64_t K, cudaStream_t s)

@@ -114,6 +114,21 @@ int bqg_repack_weights(int fmt, const void *src, void *dst, int64_t N, int64_t K
 int bqg_quantize_q8_1(const void *x, int x_dtype, void *xq, int M, int64_t K,
                       cudaStream_t stream);
 
+/* Fused RMSNorm + q8_1 quantization: the normalisation that precedes each
+ * projection folded into the activation encoder, one launch instead of two
+ * ("MI50 megakernel", hypothesis ledger: neighbouring steps fused into one
+ * dispatch).  The pages name the fusion, not its arithmetic; per row m:
+ *     s   = sum_k x[m,k]^2                 (fp64; exact for bf16 inputs)
+ *     r   = fp32( 1 / sqrt(s / K + eps) )  (fp64 square root and division)
+ *     y_k = fp32( fp32(x[m,k] * r) * gamma[k] )   (gamma NULL: no gain)
+ * then y is encoded like bqg_quantize_q8_1.  x: M x K, x_dtype BQG_BF16 or
+ * BQG_F32 (2- or 4-byte aligned); gamma: K fp32 or NULL (4-byte aligned);
+ * eps >= 0 and finite; xq: M x K/32 blocks of 36 B (4-byte aligned);
+ * 1 <= M <= 65535.  Bit-exact with that definition for bf16 inputs (for fp32
+ * inputs the fp64 sum is exact up to its last bit). */
+int bqg_rmsnorm_quantize_q8_1(const void *x, int x_dtype, const float *gamma, float eps, void *xq, int M,
+                              int64_t K, cudaStream_t stream);
+
 /* Skinny GEMV, M in {1, 2, 4, 8}.  Wp: repacked weights of the named format.
  * X: M x K bf16 (row-major).  Y: M x N fp32 (row-major).
  * ws/ws_bytes: workspace for split-K; bqg_workspace_size(op, M, N, K) bytes

@@ -89,6 +89,7 @@ class Oracle:
             "ref_gemv_f32acc": ([I, P, I, P, I64, I64, I64, P], I),
             "ref_block_dots_q4_0_q8_1": ([P, P, I64, I64, P], I),
             "ref_swiglu": ([P, P, I64, P], None),
+            "ref_rmsnorm_q8_1": ([P, P, ctypes.c_float, I64, I64, P], I),
             "ref_repacked_size": ([I, I64, I64], I64),
             "ref_repack": ([I, P, I64, I64, P], I),
             "ref_unrepack": ([I, P, I64, I64, P], I),
@@ -121,6 +122,20 @@ class Oracle:
         rc = self.L.ref_quantize(fmt, _ptr(x), rows, K, _ptr(out))
         if rc:
             raise ValueError(f"ref_quantize failed ({rc})")
+        return out
+
+    def rmsnorm_q8_1(self, x: np.ndarray, gamma=None, eps: float = 1e-5) -> np.ndarray:
+        """fp32 rows x K (bf16 inputs given exactly as fp32) -> RMS-normalised,
+        optionally scaled by gamma (K fp32), q8_1 blocks (uint8, rows x K/32*36)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim == 1:
+            x = x[None, :]
+        rows, K = x.shape
+        g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float32)
+        out = np.zeros((rows, row_bytes(Q8_1, K)), dtype=np.uint8)
+        rc = self.L.ref_rmsnorm_q8_1(_ptr(x), None if g is None else _ptr(g), ctypes.c_float(eps), rows, K, _ptr(out))
+        if rc:
+            raise ValueError(f"ref_rmsnorm_q8_1 failed ({rc})")
         return out
 
     def dequantize(self, fmt: int, data, rows: int, K: int) -> np.ndarray:

@@ -182,6 +182,40 @@ int ref_quantize(int fmt, const float *x, int64_t rows, int64_t K, uint8_t *out)
     return 0;
 }
 
+/* Fused RMSNorm -> q8_1: the normalisation that precedes each projection,
+ * folded into the activation encoder so that it is one step instead of two
+ * ([MI50] hypothesis ledger: fusing neighbouring steps and epilogues;
+ * [RX6700] Approach & Methodology: the Q8_1 activation of the matvec).
+ * Reading (the pages name the fusion, not its arithmetic), per row:
+ *     s   = sum_k x_k^2               in fp64, k in order (exact for bf16
+ *                                     inputs: each square has 16 bits)
+ *     r   = fp32( 1 / sqrt(s / K + eps) )    (fp64 sqrt and division)
+ *     y_k = fp32( fp32(x_k * r) * gamma_k )  (gamma NULL: y_k = fp32(x_k * r))
+ * and y is encoded into q8_1 blocks by encode_q8_1 above.
+ * x: rows x K fp32 (bf16 inputs are passed exactly as fp32).  out: rows x K/32
+ * blocks of 36 bytes. */
+int ref_rmsnorm_q8_1(const float *x, const float *gamma, float eps, int64_t rows, int64_t K, uint8_t *out)
+{
+    if (K <= 0 || K % QK) return -1;
+    float *y = (float *)malloc((size_t)K * sizeof(float));
+    if (!y) return -3;
+    int64_t nb = K / QK;
+    for (int64_t r = 0; r < rows; r++) {
+        const float *xr = x + r * K;
+        double s = 0.0;
+        for (int64_t k = 0; k < K; k++) s += (double)xr[k] * (double)xr[k];
+        const float rr = (float)(1.0 / sqrt(s / (double)K + (double)eps));
+        for (int64_t k = 0; k < K; k++) {
+            float v = xr[k] * rr;
+            if (gamma) v = v * gamma[k];
+            y[k] = v;
+        }
+        for (int64_t b = 0; b < nb; b++) encode_q8_1(y + b * QK, out + (r * nb + b) * Q8_1_BYTES);
+    }
+    free(y);
+    return 0;
+}
+
 /* ------------------------------------------------------------------ */
 /* Exact decoding of one row to double.                                 */
 /* ------------------------------------------------------------------ */

@@ -404,4 +404,63 @@ def pin_repack_layout(o):
     assert np.array_equal(o.repack(BF16, bf, 8, 64), bf.view(np.uint8))
 
 
+def _fp16(u: int) -> float:
+    return float(_half(struct.pack("<H", u & 0xFFFF)))
+
+
+def _bf16_values(x):
+    """fp32 array rounded to bf16 (nearest even), returned as fp32."""
+    bits = _to_bf16_bits(x).astype(np.uint32) << 16
+    return bits.view(np.float32)
+
+
+def pin_rmsnorm_q8_1_hand_block(o):
+    """The hand-worked block: a constant row normalises to ones."""
+    g = _read_golden("rmsnorm_q8_1_hand_block.txt")
+    want = _hexbytes(g["bytes"])
+    for key in ("x1", "xhalf"):
+        x = np.array([float(v) for v in g[key]], dtype=np.float32)
+        got = o.rmsnorm_q8_1(x, None, 0.0)[0]
+        assert np.array_equal(got, want), (key, bytes(got).hex())
+
+
+def pin_rmsnorm_q8_1_properties(o):
+    """Against the definition, with the sum of squares taken exactly
+    (fractions) and the square root from the math library:
+      * every dequantized output is within half a step (d/2) of
+        x_k / sqrt(mean(x^2) + eps) * gamma_k, up to the fp32 roundings of r
+        and of the two products;
+      * gamma of ones is no gamma; gamma of 2 doubles d and s and keeps the codes;
+      * a zero row (eps > 0) gives all-zero blocks."""
+    rng = np.random.default_rng(21)
+    M, K = 3, 1024
+    x = _bf16_values(rng.normal(0, 1, (M, K)).astype(np.float32))
+    for eps, gamma in ((1e-5, None), (0.5, None), (1e-6, rng.uniform(0.5, 1.5, K).astype(np.float32))):
+        out = o.rmsnorm_q8_1(x, gamma, eps)
+        deq = o.dequantize(Q8_1, out.reshape(-1), M, K)
+        for m in range(M):
+            s = sum(Fraction(float(v)) ** 2 for v in x[m])
+            inv = 1.0 / math.sqrt(float(s / K) + float(np.float32(eps)))
+            ref = x[m].astype(np.float64) * inv * (1.0 if gamma is None else gamma.astype(np.float64))
+            for b in range(K // 32):
+                blk = out[m, b * 36:(b + 1) * 36]
+                d = _fp16(int(blk[0]) | int(blk[1]) << 8)
+                err = np.abs(deq[m, b * 32:(b + 1) * 32] - ref[b * 32:(b + 1) * 32])
+                slack = 4 * 2.0 ** -24 * np.abs(ref[b * 32:(b + 1) * 32])
+                assert np.all(err <= d / 2 + slack + 1e-12), (eps, m, b, float(err.max()), d)
+    # gamma of ones == no gamma; gamma of 2 doubles the scales exactly
+    a = o.rmsnorm_q8_1(x, None, 1e-5)
+    assert np.array_equal(o.rmsnorm_q8_1(x, np.ones(K, np.float32), 1e-5), a)
+    two = o.rmsnorm_q8_1(x, np.full(K, 2.0, np.float32), 1e-5)
+    for m in range(M):
+        for b in range(K // 32):
+            ba, bt = a[m, b * 36:(b + 1) * 36], two[m, b * 36:(b + 1) * 36]
+            assert np.array_equal(ba[4:], bt[4:])
+            for off in (0, 2):
+                ha, ht = int(ba[off]) | int(ba[off + 1]) << 8, int(bt[off]) | int(bt[off + 1]) << 8
+                assert _fp16(ht) == 2 * _fp16(ha), (m, b, off)
+    z = o.rmsnorm_q8_1(np.zeros((2, 64), np.float32), None, 1e-5)
+    assert not z.any()
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

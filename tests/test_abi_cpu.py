@@ -79,6 +79,10 @@ FAKE = 0x10000  # never dereferenced: every call below fails validation first
     (lambda L: L.bqg_gemv_q4_0_q8_1_qkv(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 1, 8, 8, 64, None, 0, None), 1),
     (lambda L: L.bqg_gemv_q4_0_q8_1_gate_up_swiglu(FAKE, FAKE, FAKE, FAKE, 2, 8, 40, None, 0, None), 2),
     (lambda L: L.bqg_debug_q4_0_q8_1_block_dots(FAKE, FAKE, None, 8, 64, None), 1),
+    (lambda L: L.bqg_rmsnorm_quantize_q8_1(FAKE, 0, None, -1.0, FAKE, 1, 64, None), 1),          # eps < 0
+    (lambda L: L.bqg_rmsnorm_quantize_q8_1(FAKE, 0, None, float("nan"), FAKE, 1, 64, None), 1),  # eps NaN
+    (lambda L: L.bqg_rmsnorm_quantize_q8_1(FAKE, 0, FAKE + 2, 1e-5, FAKE, 1, 64, None), 3),     # gamma
+    (lambda L: L.bqg_rmsnorm_quantize_q8_1(FAKE, 0, None, 1e-5, FAKE, 1, 40, None), 2),         # K % 32
 ])
 def test_host_validation_rejects_before_launch(L, call, status):
     assert call(L) == status

@@ -78,6 +78,29 @@ def test_quantize_q8_1_bitexact(ora, src, M, K):
     assert np.array_equal(got.reshape(-1), want.reshape(-1))
 
 
+@pytest.mark.parametrize("src", ["bf16", "f32"])
+@pytest.mark.parametrize("gain", [False, True])
+@pytest.mark.parametrize("M,K,eps", [(1, 32, 1e-5), (1, 4096, 1e-5), (3, 1056, 1e-6), (8, 4096, 0.0),
+                                     (1, 11008, 1e-5), (2, 65536, 1e-5)])
+def test_rmsnorm_quantize_q8_1_bitexact(ora, src, gain, M, K, eps):
+    """Fused RMSNorm -> q8_1 against the oracle's definition, byte for byte."""
+    x = synth.activations_f32(M, K, seed=300 + M + K) * 2
+    if M > 1:
+        x[1] = 0.0 if eps > 0 else 1.0                  # a zero row (eps > 0) or a constant row
+    if src == "bf16":
+        bits = synth.bf16_bits(x)
+        xt = synth.bf16_tensor(bits)
+        xref = np.array(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float())
+    else:
+        xt = torch.from_numpy(x).cuda()
+        xref = x
+    g = np.random.default_rng(K).uniform(0.25, 2.0, K).astype(np.float32) if gain else None
+    gt = torch.from_numpy(g).cuda() if gain else None
+    got = bqg.rmsnorm_quantize_q8_1(xt, gt, eps).cpu().numpy()
+    want = ora.rmsnorm_q8_1(xref, g, eps)
+    assert np.array_equal(got.reshape(-1), want.reshape(-1))
+
+
 @pytest.mark.parametrize("fmt", [Q8_0, Q4_0])
 @pytest.mark.parametrize("N,K", [(1, 32), (5, 1056), (64, 4096), (3, 11008)])
 def test_quantize_weights_bitexact(ora, fmt, N, K):

@@ -33,6 +33,9 @@ MUTANTS = [
     ("repack_codes_offset", "memcpy(tile + 16 * s, blk + 2, 16);\n                memcpy(tile + 512 + 2 * s, blk, 2);",
      "memcpy(tile + 16 * s, blk, 16);\n                memcpy(tile + 512 + 2 * s, blk, 2);"),
     ("bf16_decode_shift", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    ("rmsnorm_sum_not_mean", "sqrt(s / (double)K + (double)eps)", "sqrt(s + (double)eps)"),
+    ("rmsnorm_eps_outside_root", "sqrt(s / (double)K + (double)eps)", "sqrt(s / (double)K) + (double)eps"),
+    ("rmsnorm_gamma_ignored", "if (gamma) v = v * gamma[k];", "if (gamma) v = v;"),
 ]
 
 
