@@ -268,8 +268,9 @@ class GemmArm(Arm):
 
 class DecodeLayerArm(Arm):
     """q4_0 x q8_1 decode layer: quantize(x), QKV, gate+up+SwiGLU, quantize(h), down.
-    With fused_norm the layer starts from the raw activation row and its first
-    step is the fused RMSNorm -> q8_1 encoder instead of a plain encoder."""
+    With fused_norm the layer starts from the raw activation row: its first
+    step is the fused RMSNorm -> q8_1 encoder, and the gate+up epilogue writes
+    h as q8_1 for the down projection (four launches instead of five)."""
 
     def __init__(self, seed=5, K=4096, Nq=4096, Nff=11008, fused_norm=False):
         import torch
@@ -279,9 +280,9 @@ class DecodeLayerArm(Arm):
         self.bqg, self.torch = bqg, torch
         self.fused_norm = fused_norm
         self.name = (f"q4_0 x q8_1 decode layer M=1 (QKV 3x{Nq}x{K}, gate+up 2x{Nff}x{K}, down {K}x{Nff})"
-                     + (", fused RMSNorm->q8_1" if fused_norm else ""))
+                     + (", fused RMSNorm->q8_1 and SwiGLU->q8_1" if fused_norm else ""))
         self.kernel_key = "decode_layer_q4_0_q8_1" + ("_fused_norm" if fused_norm else "")
-        self.launches_per_call = 5
+        self.launches_per_call = 4 if fused_norm else 5
         self.K, self.Nq, self.Nff = K, Nq, Nff
 
         def mk(N, KK, sd):
@@ -304,7 +305,8 @@ class DecodeLayerArm(Arm):
                       "hq": torch.empty((1, (Nff // 32) * 36), dtype=torch.uint8, device="cuda"),
                       "y": torch.empty((1, K), device="cuda"),
                       "ws_qkv": bqg.workspace(bqg.OP_QKV_Q4_0_Q8_1, 1, 3 * Nq, K),
-                      "ws_gu": bqg.workspace(bqg.OP_GATE_UP_Q4_0_Q8_1, 1, Nff, K),
+                      "ws_gu": bqg.workspace(bqg.OP_GATE_UP_Q8_1_Q4_0_Q8_1 if fused_norm else
+                                             bqg.OP_GATE_UP_Q4_0_Q8_1, 1, Nff, K),
                       "ws_d": bqg.workspace(bqg.OP_GEMV_Q4_0_Q8_1, 1, K, Nff)})
             self.sets.append(s)
         self.x_host = x.cpu().pin_memory()
@@ -318,8 +320,12 @@ class DecodeLayerArm(Arm):
             b.quantize_q8_1(s["x"], out=s["xq"])
         b.gemv_q4_0_q8_1_qkv(s["Wq"], s["Wk"], s["Wv"], s["xq"], self.Nq, self.Nq, self.K,
                              out=(s["q"], s["k"], s["v"]), ws=s["ws_qkv"])
-        b.gemv_q4_0_q8_1_gate_up_swiglu(s["Wg"], s["Wu"], s["xq"], self.Nff, self.K, out=s["h"], ws=s["ws_gu"])
-        b.quantize_q8_1(s["h"], out=s["hq"])
+        if self.fused_norm:
+            b.gemv_q4_0_q8_1_gate_up_swiglu_q8_1(s["Wg"], s["Wu"], s["xq"], self.Nff, self.K, out=s["hq"],
+                                                 ws=s["ws_gu"])
+        else:
+            b.gemv_q4_0_q8_1_gate_up_swiglu(s["Wg"], s["Wu"], s["xq"], self.Nff, self.K, out=s["h"], ws=s["ws_gu"])
+            b.quantize_q8_1(s["h"], out=s["hq"])
         b.gemv_q4_0_q8_1(s["Wd"], s["hq"], self.K, self.Nff, out=s["y"], ws=s["ws_d"])
 
     def call_e2e(self, i):

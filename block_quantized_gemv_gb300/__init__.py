@@ -18,6 +18,7 @@ import torch
 BF16, Q8_0, Q4_0, Q8_1, F32 = 0, 1, 2, 3, 4
 OP_GEMV_BF16, OP_GEMV_Q8_0, OP_GEMV_Q4_0, OP_GEMV_Q4_0_Q8_1 = 0, 1, 2, 3
 OP_QKV_Q4_0_Q8_1, OP_GATE_UP_Q4_0_Q8_1, OP_GEMM_Q4_0_BF16 = 4, 5, 6
+OP_GATE_UP_Q8_1_Q4_0_Q8_1 = 7
 BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q8_1: 36}
 QK = 32
 
@@ -37,6 +38,7 @@ EXPORTS = {
     "bqg_gemv_q4_0_q8_1": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemv_q4_0_q8_1_qkv": (["p", "p", "p", "p", "p", "p", "p", "i", "i64", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemv_q4_0_q8_1_gate_up_swiglu": (["p", "p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1": (["p", "p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemm_q4_0_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_debug_q4_0_q8_1_block_dots": (["p", "p", "p", "i64", "i64", "p"], "i"),
     "bqg_workspace_size": (["i", "i", "i64", "i64"], "size"),
@@ -248,6 +250,21 @@ def gemv_q4_0_q8_1_gate_up_swiglu(Wg, Wu, Xq, N, K, out=None, ws=None, stream=No
     return out
 
 
+def gemv_q4_0_q8_1_gate_up_swiglu_q8_1(Wg, Wu, Xq, N, K, out=None, ws=None, stream=None):
+    """gate+up+SwiGLU writing h as q8_1 blocks (uint8, M x N/32*36).  `ws`
+    (workspace(OP_GATE_UP_Q8_1_Q4_0_Q8_1, ...)) must start zero-filled."""
+    M = Xq.shape[0]
+    if out is None:
+        out = torch.empty((M, row_bytes(Q8_1, N)), dtype=torch.uint8, device=Xq.device)
+    wsp, wsb = _ws(ws)
+    _check(load().bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(_dev(Wg, "Wg"), _dev(Wu, "Wu"),
+                                                         _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
+                                                         _dev(out, "Hq", numel=M * row_bytes(Q8_1, N)), M, N, K,
+                                                         wsp, wsb, _stream(stream)),
+           "bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1")
+    return out
+
+
 def gemm_q4_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
     M = X.shape[0]
     if out is None:
@@ -274,8 +291,9 @@ def workspace_size(op: int, M: int, N: int, K: int) -> int:
 
 
 def workspace(op: int, M: int, N: int, K: int, device="cuda") -> torch.Tensor | None:
+    """A workspace for `op` (zero-filled, as the q8_1-output SwiGLU requires)."""
     n = workspace_size(op, M, N, K)
-    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
 
 
 def last_device_error(stream=None) -> int:

@@ -385,8 +385,15 @@ int plan_any(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
 }
 
 // Common path of every GEMV entry point.
+// Workspace of a SwiGLU call with a q8_1 output and no split-K: fp32 staging
+// of the M x N outputs, then one int32 arrival counter per q8_1 block.
+size_t swiglu_q8_1_staging(int M, int64_t N)
+{
+    return ((size_t)M * N * 4 + 15) / 16 * 16 + (size_t)M * (N / 32) * 4;
+}
+
 int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void *ws, size_t ws_bytes,
-             cudaStream_t stream)
+             cudaStream_t stream, uint8_t *hq = nullptr)
 {
     DevInfo dev;
     int dv = 0;
@@ -398,9 +405,17 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     GemvPlan g;
     st = plan_any(wf, xf, M, p.Nv, K, unit, dev, dv, &g);
     if (st) return st;
-    if (g.ws_bytes > 0) {
-        if (!ws || ws_bytes < g.ws_bytes) return BQG_ERR_WORKSPACE;
+    const size_t need = (hq && g.splits == 1) ? swiglu_q8_1_staging(M, p.rows[0]) : g.ws_bytes;
+    if (need > 0) {
+        if (!ws || ws_bytes < need) return BQG_ERR_WORKSPACE;
         if (!aligned16(ws)) return BQG_ERR_MISALIGNED;
+    }
+    if (hq) {
+        p.hq = hq;
+        if (g.splits == 1) {
+            p.Y[0] = static_cast<float *>(ws);
+            p.cnt = reinterpret_cast<int *>(static_cast<uint8_t *>(ws) + ((size_t)M * p.rows[0] * 4 + 15) / 16 * 16);
+        }
     }
     p.K = (int)K;
     p.nb = (int)(K / QK);
@@ -424,7 +439,7 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     p.rl = g.rl;
     p.piece_chunks = g.piece_chunks;
     p.x_row_bytes = g.x_row_bytes;
-    p.ws = (float *)ws;
+    p.ws = (g.splits > 1) ? (float *)ws : nullptr;
     p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;
     const bool pdl = g_pdl.load() != 0;
     cudaError_t e = g.lpr ? lpr_runner(wf, xf)(p, M, g.grid, g.threads, g.smem, stream, pdl, nullptr)
@@ -600,6 +615,23 @@ int bqg_gemv_q4_0_q8_1_gate_up_swiglu(const void *Wg, const void *Wu, const void
     return run_gemv(W_Q4_0, X_Q8_1, p, M, K, EPI_SWIGLU, ws, ws_bytes, stream);
 }
 
+int bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(const void *Wg, const void *Wu, const void *Xq, void *Hq, int M,
+                                           int64_t N, int64_t K, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!Wg || !Wu || !Xq || !Hq || N < 0 || !valid_m(M)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (N % QK) return BQG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(Wg) || !aligned16(Wu) || !aligned(Xq, 4) || !aligned(Hq, 4)) return BQG_ERR_MISALIGNED;
+    GemvParams p{};
+    p.W[0] = (const uint8_t *)Wg; p.W[1] = (const uint8_t *)Wu;
+    p.rows[0] = N; p.rows[1] = N;
+    p.nmat = 2;
+    p.X = (const uint8_t *)Xq;
+    p.Nv = 2 * N;
+    p.row_bytes = repacked_row_bytes(BQG_Q4_0, K);
+    return run_gemv(W_Q4_0, X_Q8_1, p, M, K, EPI_SWIGLU, ws, ws_bytes, stream, (uint8_t *)Hq);
+}
+
 int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws,
                        size_t ws_bytes, cudaStream_t stream)
 {
@@ -643,10 +675,12 @@ size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K)
     case BQG_OP_GEMV_Q4_0_Q8_1: break;
     case BQG_OP_QKV_Q4_0_Q8_1: break;
     case BQG_OP_GATE_UP_Q4_0_Q8_1: Nv = 2 * N; unit = 2; break;
+    case BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1: Nv = 2 * N; unit = 2; break;
     default: return 0;
     }
     GemvPlan g;
     if (plan_any(wf, xf, M, Nv, K, unit, dev, dv, &g) != BQG_OK) return 0;
+    if (op == BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1 && g.splits == 1) return N % QK ? 0 : swiglu_q8_1_staging(M, N);
     return g.ws_bytes;
 }
 

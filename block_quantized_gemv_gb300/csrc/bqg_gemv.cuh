@@ -76,10 +76,66 @@ struct GemvParams {
     int early;              // stages per warp requested before waiting for the previous grid
     int rl;                 // rows per lane (lanes-per-row kernel: 1, 2 or 4)
     int piece_chunks;       // chunks per K-piece (lanes-per-row kernel)
+    // SwiGLU with a q8_1 output: the blocks go to hq (M x rows[0]/32 blocks);
+    // Y[0] is then an fp32 staging row set and cnt one arrival counter per
+    // block (zero between calls)
+    uint8_t *hq;
+    int *cnt;
 };
 
 // Error word set when a bounded wait gives up (one per translation unit).
 static __device__ int g_gemv_error;
+
+// ---------------------------------------------------------------------------
+// SwiGLU epilogue with a q8_1 output.  The 32 outputs of a block are finished
+// by different warps and CTAs, so each output is stored in fp32 and counted
+// at its block (the store is made visible first); the arrival that completes
+// the block encodes it from L2 and re-arms the counter for the next call.
+// Nothing waits on another CTA.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool swiglu_store(const GemvParams &p, int m, int64_t o, float h)
+{
+    p.Y[0][(int64_t)m * p.rows[0] + o] = h;
+    if (!p.hq) return false;
+    __threadfence();
+    return atomicAdd(p.cnt + (int64_t)m * (p.rows[0] / 32) + o / 32, 1) == 31;
+}
+// warp-wide: encode block b of activation row m
+__device__ __forceinline__ void swiglu_encode_block_warp(const GemvParams &p, int m, int64_t b, int lane)
+{
+    __threadfence();
+    const int64_t blk = (int64_t)m * (p.rows[0] / 32) + b;
+    const float v = __ldcg(p.Y[0] + (int64_t)m * p.rows[0] + b * 32 + lane);
+    q8_1_encode_warp(v, lane, p.hq + blk * Q8_1_BYTES);
+    if (lane == 0) p.cnt[blk] = 0;
+}
+// one thread: the same encoding, element by element
+__device__ __forceinline__ void swiglu_encode_block_thread(const GemvParams &p, int m, int64_t b)
+{
+    __threadfence();
+    const int64_t blk = (int64_t)m * (p.rows[0] / 32) + b;
+    const float *h = p.Y[0] + (int64_t)m * p.rows[0] + b * 32;
+    float v[32];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; i++) {
+        v[i] = __ldcg(h + i);
+        amax = fmaxf(amax, fabsf(v[i]));
+    }
+    const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    const float d = __half2float(dh);
+    uint8_t *out = p.hq + blk * Q8_1_BYTES;
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 32; i++) {
+        const int q = q8_code(v[i], d);
+        sum += q;
+        out[4 + i] = (uint8_t)(int8_t)q;
+    }
+    const __half sh = __float2half_rn(d * (float)sum);
+    *reinterpret_cast<uint32_t *>(out) = (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(sh) << 16);
+    p.cnt[blk] = 0;
+}
 
 // Virtual row -> (matrix, row in matrix)
 __device__ __forceinline__ void map_row(const GemvParams &p, int64_t v, int &mat, int64_t &r)
@@ -584,7 +640,8 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
                         gs += part[((2 * pr) * WPG + w) * M + m];
                         us += part[((2 * pr + 1) * WPG + w) * M + m];
                     }
-                    p.Y[0][(int64_t)m * p.rows[0] + ((win0 >> 1) + pr)] = silu(gs) * us;
+                    const int64_t o = (win0 >> 1) + pr;
+                    if (swiglu_store(p, m, o, silu(gs) * us)) swiglu_encode_block_thread(p, m, o / 32);
                 }
             } else {
                 for (int t = tid; t < nrw * M; t += ncons) {
@@ -1035,18 +1092,23 @@ __global__ void __launch_bounds__(384, 2) gemv_lpr_kernel(const GemvParams p)
                 tot[i][m] = a;
                 acc[i][m][0] = acc[i][m][1] = 0.f;
             }
-        if (lane != 0 || !ok) continue;
         if (swiglu) {
             // rows 0 .. RL/2-1 are gates, RL/2 .. RL-1 the matching ups
 #pragma unroll
             for (int k = 0; k < RL / 2; k++) {
                 const int64_t v = staged_vrow(p, vb, RL, k);
-                if (v >= v1) continue;
+                const bool valid = ok && v < v1;
 #pragma unroll
-                for (int m = 0; m < M; m++)
-                    p.Y[0][(int64_t)m * p.rows[0] + (v >> 1)] = silu(tot[k][m]) * tot[RL / 2 + k][m];
+                for (int m = 0; m < M; m++) {
+                    bool last = false;
+                    if (lane == 0 && valid) last = swiglu_store(p, m, v >> 1, silu(tot[k][m]) * tot[RL / 2 + k][m]);
+                    if (__shfl_sync(0xffffffffu, (int)last, 0)) swiglu_encode_block_warp(p, m, (v >> 1) / 32, lane);
+                }
             }
-        } else {
+            continue;
+        }
+        if (lane != 0 || !ok) continue;
+        {
 #pragma unroll
             for (int i = 0; i < RL; i++) {
                 const int64_t v = staged_vrow(p, vb, RL, i);
@@ -1132,7 +1194,13 @@ static __global__ void __launch_bounds__(256) gemv_splitk_reduce(const GemvParam
             gs += p.ws[((int64_t)s * M + m) * p.Nv + 2 * pr];
             us += p.ws[((int64_t)s * M + m) * p.Nv + 2 * pr + 1];
         }
-        p.Y[0][m * p.rows[0] + pr] = silu(gs) * us;
+        const float h = silu(gs) * us;
+        if (p.hq) {
+            // np % 32 == 0: the warp holds exactly block i / 32 of row m
+            q8_1_encode_warp(h, threadIdx.x & 31, p.hq + (i / 32) * Q8_1_BYTES);
+        } else {
+            p.Y[0][m * p.rows[0] + pr] = h;
+        }
     } else {
         if (i >= (int64_t)M * p.Nv) return;
         const int64_t m = i / p.Nv, v = i - (i / p.Nv) * p.Nv;

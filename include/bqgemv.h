@@ -84,7 +84,8 @@ enum {
     BQG_OP_GEMV_Q4_0_Q8_1 = 3,
     BQG_OP_QKV_Q4_0_Q8_1 = 4,       /* N = Nq + 2*Nkv */
     BQG_OP_GATE_UP_Q4_0_Q8_1 = 5,   /* N = rows of each of gate and up */
-    BQG_OP_GEMM_Q4_0_BF16 = 6
+    BQG_OP_GEMM_Q4_0_BF16 = 6,
+    BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1 = 7 /* gate+up SwiGLU with q8_1 output; N = rows of each */
 };
 
 /* ---- load time ------------------------------------------------------- */
@@ -187,6 +188,25 @@ int bqg_gemv_q4_0_q8_1_qkv(const void *Wq, const void *Wk, const void *Wv, const
 int bqg_gemv_q4_0_q8_1_gate_up_swiglu(const void *Wg, const void *Wu, const void *Xq, float *H,
                                       int M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
                                       cudaStream_t stream);
+
+/* The same gate+up+SwiGLU whose epilogue writes h as q8_1 blocks, ready for
+ * the down projection (bqg_gemv_q4_0_q8_1 at K = N), instead of fp32: the
+ * standalone encoder between the two launches goes away ("rx-6700xt-
+ * llama2-decode", Approach & Methodology: the fused gate+up writes the
+ * SwiGLU result directly).  Hq: M x N/32 blocks of 36 B (4-byte aligned);
+ * N must be a multiple of 32.  Each block is encoded, with the rules of
+ * bqg_quantize_q8_1, from the fp32 values h = silu(g) * u that
+ * bqg_gemv_q4_0_q8_1_gate_up_swiglu would write, so the two agree byte for
+ * byte with bqg_quantize_q8_1 applied to the latter.
+ * ws: bqg_workspace_size(BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1, M, N, K) bytes,
+ * 16-byte aligned.  Without split-K it holds an fp32 staging copy of h and
+ * one counter per block, which must be ZERO before the first call on that
+ * workspace (every successful call leaves them zero; after a
+ * BQG_ERR_TIMEOUT report, zero them again).  Calls that share a workspace
+ * must not overlap. */
+int bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(const void *Wg, const void *Wu, const void *Xq, void *Hq, int M,
+                                           int64_t N, int64_t K, void *ws, size_t ws_bytes,
+                                           cudaStream_t stream);
 
 /* Prefill GEMM ("llama-3x-prompt-speed", "the tile"): each weight tile is
  * dequantized once to bf16 ((q-8)*d rounded to nearest-even bf16) in shared

@@ -83,6 +83,8 @@ FAKE = 0x10000  # never dereferenced: every call below fails validation first
     (lambda L: L.bqg_rmsnorm_quantize_q8_1(FAKE, 0, None, float("nan"), FAKE, 1, 64, None), 1),  # eps NaN
     (lambda L: L.bqg_rmsnorm_quantize_q8_1(FAKE, 0, FAKE + 2, 1e-5, FAKE, 1, 64, None), 3),     # gamma
     (lambda L: L.bqg_rmsnorm_quantize_q8_1(FAKE, 0, None, 1e-5, FAKE, 1, 40, None), 2),         # K % 32
+    (lambda L: L.bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(FAKE, FAKE, FAKE, FAKE, 1, 40, 64, None, 0, None), 2),  # N % 32
+    (lambda L: L.bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(FAKE, FAKE, FAKE, FAKE + 2, 1, 64, 64, None, 0, None), 3),
 ])
 def test_host_validation_rejects_before_launch(L, call, status):
     assert call(L) == status

@@ -264,6 +264,37 @@ def test_gate_up_swiglu(ora, M, N, K):
     assert np.all(np.abs(h - h_ref) <= bound), float(np.max(np.abs(h - h_ref) / bound))
 
 
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("N,K", [(64, 1024), (11008, 4096), (32, 11008), (4096, 4096)])
+def test_gate_up_swiglu_q8_1(ora, M, N, K):
+    """SwiGLU epilogue writing q8_1: (1) byte for byte the q8_1 encoding of the
+    fp32 h the plain entry point writes; (2) within the SwiGLU bound plus half
+    a quantization step of the oracle's h; (3) the workspace's block counters
+    are re-armed, so a second call gives the same bytes."""
+    _, cg = make_weights(ora, Q4_0, N, K, seed=41)
+    _, cu = make_weights(ora, Q4_0, N, K, seed=42)
+    xq = ora.quantize(Q8_1, synth.rms_normalised_f32(M, K, seed=43))
+    Wg, Wu = gpu_repacked(Q4_0, cg, N, K), gpu_repacked(Q4_0, cu, N, K)
+    xt = synth.u8_tensor(xq).view(M, -1)
+    ws = bqg.workspace(bqg.OP_GATE_UP_Q8_1_Q4_0_Q8_1, M, N, K)
+    Hq = bqg.gemv_q4_0_q8_1_gate_up_swiglu_q8_1(Wg, Wu, xt, N, K, ws=ws)
+    Hq2 = bqg.gemv_q4_0_q8_1_gate_up_swiglu_q8_1(Wg, Wu, xt, N, K, ws=ws)
+    H = bqg.gemv_q4_0_q8_1_gate_up_swiglu(Wg, Wu, xt, N, K, ws=bqg.workspace(bqg.OP_GATE_UP_Q4_0_Q8_1, M, N, K))
+    torch.cuda.synchronize()
+    got = Hq.cpu().numpy().reshape(-1)
+    assert np.array_equal(ora.quantize(Q8_1, H.cpu().numpy()).reshape(-1), got)
+    assert np.array_equal(Hq2.cpu().numpy().reshape(-1), got)
+    Yg, Ag = ora.gemv(Q4_0, cg, Q8_1, xq, M, N, K, nthreads=8)
+    Yu, Au = ora.gemv(Q4_0, cu, Q8_1, xq, M, N, K, nthreads=8)
+    h_ref, bound = swiglu_bound(ora, Yg, Ag, Yu, Au)
+    deq = ora.dequantize(Q8_1, got, M, N)
+    blocks = got.reshape(M, N // 32, 36)
+    d = np.frombuffer(blocks[:, :, 0:2].copy().tobytes(), dtype=np.float16).astype(np.float64).reshape(M, N // 32)
+    half_step = np.repeat(d / 2, 32, axis=1)
+    assert np.all(np.abs(deq - h_ref) <= bound + half_step * (1 + 2.0 ** -10)), \
+        float(np.max(np.abs(deq - h_ref) - bound - half_step))
+
+
 # ---------------------------------------------------------------------------
 # error paths on a real device (nothing is launched)
 # ---------------------------------------------------------------------------
