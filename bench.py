@@ -232,18 +232,21 @@ class GemvArm(Arm):
 
 
 class GemmArm(Arm):
-    """Prefill GEMM M=512 (bf16 activations) x q4_0 weights."""
+    """Prefill GEMM M=512 (bf16 activations) x q4_0 (or q8_0) weights."""
 
-    def __init__(self, M=512, N=14336, K=4096, seed=9, sets=None):
+    def __init__(self, M=512, N=14336, K=4096, seed=9, sets=None, fmt=None):
         import torch
         import block_quantized_gemv_gb300 as bqg
         from block_quantized_gemv_gb300 import synth
         super().__init__()
         self.bqg, self.M, self.N, self.K = bqg, M, N, K
-        self.name = f"q4_0 x bf16 prefill GEMM M={M} K={K} N={N}"
-        self.kernel_key = f"gemm_q4_0_bf16_M{M}_K{K}_N{N}"
+        fmt = bqg.Q4_0 if fmt is None else fmt
+        fname = "q8_0" if fmt == bqg.Q8_0 else "q4_0"
+        self.fn = bqg.gemm_q8_0_bf16 if fmt == bqg.Q8_0 else bqg.gemm_q4_0_bf16
+        self.name = f"{fname} x bf16 prefill GEMM M={M} K={K} N={N}"
+        self.kernel_key = f"gemm_{fname}_bf16_M{M}_K{K}_N{N}"
         Wf = torch.from_numpy(synth.weights_f32(N, K, seed)).cuda()
-        Wp = bqg.repack_weights(bqg.Q4_0, bqg.quantize_weights(bqg.Q4_0, Wf), N, K)
+        Wp = bqg.repack_weights(fmt, bqg.quantize_weights(fmt, Wf), N, K)
         del Wf
         X = torch.from_numpy(synth.activations_f32(M, K, seed + 1)).cuda().to(torch.bfloat16)
         self.bytes_per_call = Wp.numel() + X.numel() * 2 + M * N * 4
@@ -257,7 +260,7 @@ class GemmArm(Arm):
 
     def call(self, i):
         s = self.sets[i % self.R]
-        self.bqg.gemm_q4_0_bf16(s["W"], s["X"], self.N, self.K, out=s["Y"])
+        self.fn(s["W"], s["X"], self.N, self.K, out=s["Y"])
 
     def call_e2e(self, i):
         s = self.sets[i % self.R]
@@ -573,7 +576,8 @@ def main():
     other = [GemvArm(bqg.Q8_0, bqg.BF16, 1, N_HEAD, K_HEAD), GemvArm(bqg.Q4_0, bqg.Q8_1, 1, N_HEAD, K_HEAD),
              GemmArm()]
     if args.suite == "full":
-        other += [GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096), DecodeLayerArm(), DecodeLayerArm(fused_norm=True)]
+        other += [GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096), DecodeLayerArm(), DecodeLayerArm(fused_norm=True),
+                  GemmArm(fmt=bqg.Q8_0)]
         for M in (1, 2, 4, 8):
             for f in (bqg.BF16, bqg.Q8_0, bqg.Q4_0):
                 other.append(GemvArm(f, bqg.BF16, M, 14336, 4096))

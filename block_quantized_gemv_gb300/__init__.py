@@ -18,7 +18,7 @@ import torch
 BF16, Q8_0, Q4_0, Q8_1, F32 = 0, 1, 2, 3, 4
 OP_GEMV_BF16, OP_GEMV_Q8_0, OP_GEMV_Q4_0, OP_GEMV_Q4_0_Q8_1 = 0, 1, 2, 3
 OP_QKV_Q4_0_Q8_1, OP_GATE_UP_Q4_0_Q8_1, OP_GEMM_Q4_0_BF16 = 4, 5, 6
-OP_GATE_UP_Q8_1_Q4_0_Q8_1 = 7
+OP_GATE_UP_Q8_1_Q4_0_Q8_1, OP_GEMM_Q8_0_BF16 = 7, 8
 BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q8_1: 36}
 QK = 32
 
@@ -40,6 +40,7 @@ EXPORTS = {
     "bqg_gemv_q4_0_q8_1_gate_up_swiglu": (["p", "p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1": (["p", "p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemm_q4_0_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_gemm_q8_0_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_debug_q4_0_q8_1_block_dots": (["p", "p", "p", "i64", "i64", "p"], "i"),
     "bqg_workspace_size": (["i", "i", "i64", "i64"], "size"),
     "bqg_last_device_error": (["p", "p"], "i"),
@@ -273,6 +274,17 @@ def gemm_q4_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
     _check(load().bqg_gemm_q4_0_bf16(_dev(Wp, "Wp"), _dev(X, "X", torch.bfloat16, M * K * 2),
                                      _dev(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)),
            "bqg_gemm_q4_0_bf16")
+    return out
+
+
+def gemm_q8_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
+    M = X.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    wsp, wsb = _ws(ws)
+    _check(load().bqg_gemm_q8_0_bf16(_dev(Wp, "Wp"), _dev(X, "X", torch.bfloat16, M * K * 2),
+                                     _dev(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)),
+           "bqg_gemm_q8_0_bf16")
     return out
 
 

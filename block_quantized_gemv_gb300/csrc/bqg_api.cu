@@ -34,7 +34,7 @@ cudaError_t launch_quantize_weights(int, const float *, void *, int64_t, int64_t
 cudaError_t launch_repack(int, const void *, void *, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_block_dots(const void *, const void *, int32_t *, int64_t, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_splitk_reduce(const GemvParams &, int, int, int, cudaStream_t, bool);
-int gemm_q4_0_bf16(const void *, const void *, float *, int, int64_t, int64_t, cudaStream_t, int);
+int gemm_bf16(int, const void *, const void *, float *, int, int64_t, int64_t, cudaStream_t, int);
 size_t gemm_workspace(int, int64_t, int64_t);
 int gemm_read_error(cudaStream_t, int *);
 }  // namespace bqg
@@ -632,8 +632,8 @@ int bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(const void *Wg, const void *Wu, const
     return run_gemv(W_Q4_0, X_Q8_1, p, M, K, EPI_SWIGLU, ws, ws_bytes, stream, (uint8_t *)Hq);
 }
 
-int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws,
-                       size_t ws_bytes, cudaStream_t stream)
+static int gemm_entry(int fmt, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws,
+                      size_t ws_bytes, cudaStream_t stream)
 {
     (void)ws; (void)ws_bytes;
     if (!Wp || !X || !Y || M <= 0 || N < 0) return BQG_ERR_INVALID_ARG;
@@ -642,7 +642,19 @@ int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N
     DevInfo dev;
     if (int st = current_device(&dev)) return st;
     if (N == 0) return BQG_OK;
-    return gemm_q4_0_bf16(Wp, X, Y, M, N, K, stream, dev.sms);
+    return gemm_bf16(fmt, Wp, X, Y, M, N, K, stream, dev.sms);
+}
+
+int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws,
+                       size_t ws_bytes, cudaStream_t stream)
+{
+    return gemm_entry(BQG_Q4_0, Wp, X, Y, M, N, K, ws, ws_bytes, stream);
+}
+
+int bqg_gemm_q8_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws,
+                       size_t ws_bytes, cudaStream_t stream)
+{
+    return gemm_entry(BQG_Q8_0, Wp, X, Y, M, N, K, ws, ws_bytes, stream);
 }
 
 int bqg_debug_q4_0_q8_1_block_dots(const void *Wp, const void *Xq, int32_t *dots, int64_t N, int64_t K,
@@ -660,7 +672,7 @@ int bqg_debug_q4_0_q8_1_block_dots(const void *Wp, const void *Xq, int32_t *dots
 size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K)
 {
     if (N <= 0 || K <= 0 || K % QK || K > kMaxK) return 0;
-    if (op == BQG_OP_GEMM_Q4_0_BF16) return gemm_workspace(M, N, K);
+    if (op == BQG_OP_GEMM_Q4_0_BF16 || op == BQG_OP_GEMM_Q8_0_BF16) return gemm_workspace(M, N, K);
     if (!valid_m(M)) return 0;
     DevInfo dev;
     int dv = 0;

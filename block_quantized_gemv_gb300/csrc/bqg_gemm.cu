@@ -57,7 +57,6 @@ constexpr int DQ_WARPS = 8;                   // dequantizing warps (1..8)
 constexpr int EPI_WARP0 = 1 + DQ_WARPS;       // epilogue warps 9..12
 constexpr int TMA_WARP = EPI_WARP0 + 4;       // activation loads: warp 13
 constexpr int NUM_THREADS = (TMA_WARP + 1) * 32;
-constexpr int PREFETCH = 8;                   // k-steps of weight codes in flight per thread
 
 // shared memory map (dynamic, 1024-byte aligned)
 constexpr int OFF_STAGES = 0;
@@ -164,6 +163,66 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, int shift, f
                       pack_bf16x2(f[6], f[7]));
 }
 
+// 8 dequantized q8_0 weights q * d of one word pair (bytes = codes 4i..4i+7),
+// as 4 bf16x2 words
+__device__ __forceinline__ uint4 dequant8_q8(uint32_t w0, uint32_t w1, float d)
+{
+    constexpr float OFF = 8388608.0f + 128.0f;
+    const uint32_t a = w0 ^ 0x80808080u, b = w1 ^ 0x80808080u;   // q + 128 as unsigned bytes
+    float f[8] = {byte_plus_2p23<0>(a), byte_plus_2p23<1>(a), byte_plus_2p23<2>(a), byte_plus_2p23<3>(a),
+                  byte_plus_2p23<0>(b), byte_plus_2p23<1>(b), byte_plus_2p23<2>(b), byte_plus_2p23<3>(b)};
+#pragma unroll
+    for (int i = 0; i < 8; i++) f[i] = (f[i] - OFF) * d;     // exact: 8-bit integer times an fp16 value
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+// One weight block's codes and scale as a dequantizing thread holds them, and
+// the repacked-tile addresses they come from (include/bqgemv.h).
+template <int WF> struct BlockCodes;
+template <> struct BlockCodes<BQG_Q4_0> {
+    static constexpr int TILE = Q4_0_TILE;
+    static constexpr int PREFETCH = 8;       // k-steps of codes in flight per thread
+    uint4 c;
+    uint32_t s;
+    __device__ __forceinline__ void load(const uint8_t *tile, int s_)
+    {
+        c = ldg_v4(tile + 16 * s_);
+        s = __ldg(reinterpret_cast<const unsigned short *>(tile + 512 + 2 * s_));
+    }
+    __device__ __forceinline__ void clear() { c = make_uint4(0, 0, 0, 0); s = 0; }
+    // block elements 0..31 -> v[0..3] (8 each): low nibbles are 0..15, high 16..31
+    __device__ __forceinline__ void dequant(uint4 (&v)[4]) const
+    {
+        const float d = half_bits_to_float(s);
+        v[0] = dequant8(c.x, c.y, 0, d);
+        v[1] = dequant8(c.z, c.w, 0, d);
+        v[2] = dequant8(c.x, c.y, 4, d);
+        v[3] = dequant8(c.z, c.w, 4, d);
+    }
+};
+template <> struct BlockCodes<BQG_Q8_0> {
+    static constexpr int TILE = Q8_0_TILE;
+    static constexpr int PREFETCH = 4;
+    uint4 lo, hi;
+    uint32_t s;
+    __device__ __forceinline__ void load(const uint8_t *tile, int s_)
+    {
+        lo = ldg_v4(tile + 16 * s_);
+        hi = ldg_v4(tile + 512 + 16 * s_);
+        s = __ldg(reinterpret_cast<const unsigned short *>(tile + 1024 + 2 * s_));
+    }
+    __device__ __forceinline__ void clear() { lo = hi = make_uint4(0, 0, 0, 0); s = 0; }
+    __device__ __forceinline__ void dequant(uint4 (&v)[4]) const
+    {
+        const float d = half_bits_to_float(s);
+        v[0] = dequant8_q8(lo.x, lo.y, d);
+        v[1] = dequant8_q8(lo.z, lo.w, d);
+        v[2] = dequant8_q8(hi.x, hi.y, d);
+        v[3] = dequant8_q8(hi.z, hi.w, d);
+    }
+};
+
 struct GemmArgs {
     const uint8_t *W;       // repacked q4_0, N rows
     float *Y;               // M x N
@@ -173,7 +232,8 @@ struct GemmArgs {
     int tiles_n;            // N / TM
 };
 
-__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __grid_constant__ CUtensorMap xmap,
+template <int WF>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                         const GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -291,24 +351,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
             const int tn = u % a.tiles_n;
             const uint8_t *row = a.W + (int64_t)(tn * TM + r) * a.row_bytes;
-            // block 2k + h of this row: 16 code bytes and its fp16 scale
-            auto load = [&](int k, uint4 &c, uint32_t &sc) {
+            // block 2k + h of this row: its codes and fp16 scale
+            auto load = [&](int k, BlockCodes<WF> &c) {
                 if (k >= nk) return;
                 const int blk = 2 * k + h;
-                const uint8_t *tile = row + (int64_t)(blk >> 5) * Q4_0_TILE;
-                c = ldg_v4(tile + 16 * (blk & 31));
-                sc = __ldg(reinterpret_cast<const unsigned short *>(tile + 512 + 2 * (blk & 31)));
+                c.load(row + (int64_t)(blk >> 5) * BlockCodes<WF>::TILE, blk & 31);
             };
             // ring of PREFETCH k-steps of codes and scales in registers; the loop
             // is unrolled by PREFETCH so each slot is reloaded right after use
             // and never moved while its load is in flight
-            uint4 cr[PREFETCH];
-            uint32_t sr[PREFETCH];
+            constexpr int PREFETCH = BlockCodes<WF>::PREFETCH;
+            BlockCodes<WF> cr[PREFETCH];
 #pragma unroll
             for (int i = 0; i < PREFETCH; i++) {
-                cr[i] = make_uint4(0, 0, 0, 0);
-                sr[i] = 0;
-                load(i, cr[i], sr[i]);
+                cr[i].clear();
+                load(i, cr[i]);
             }
             for (int k0 = 0; k0 < nk && ok; k0 += PREFETCH) {
 #pragma unroll
@@ -321,12 +378,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_q4_0_bf16_kernel(const __
                     const bool free_slot = step < NSTAGE || mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1);
                     if (!__all_sync(0xffffffffu, free_slot)) { fail(); ok = false; break; }
                     if (*abort_flag) { ok = false; break; }
-                    const uint4 c0 = cr[i];
-                    const float d = half_bits_to_float(sr[i]);
-                    load(k + PREFETCH, cr[i], sr[i]);
                     // block h covers k 32h .. 32h+31 of the step: 16 columns of the slot
-                    const uint4 v[4] = {dequant8(c0.x, c0.y, 0, d), dequant8(c0.z, c0.w, 0, d),
-                                        dequant8(c0.x, c0.y, 4, d), dequant8(c0.z, c0.w, 4, d)};
+                    uint4 v[4];
+                    cr[i].dequant(v);
+                    load(k + PREFETCH, cr[i]);
                     tmem_st16(arow + s * A_COLS, v);
                     tc_fence_before();                             // tensor-memory writes -> the MMA thread
                     __syncwarp();
@@ -396,8 +451,9 @@ int gemm_read_error(cudaStream_t stream, int *out)
 
 size_t gemm_workspace(int, int64_t, int64_t) { return 0; }
 
-// M % 128 == 0, N % 128 == 0, K % 64 == 0 (checked by the caller)
-int gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, cudaStream_t stream, int sms)
+// M % 128 == 0, N % 128 == 0, K % 64 == 0 (checked by the caller); wf: BQG_Q4_0 or BQG_Q8_0
+int gemm_bf16(int wf, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, cudaStream_t stream,
+              int sms)
 {
     static std::mutex mu;
     auto enc = encode_fn();
@@ -415,7 +471,7 @@ int gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, in
     a.W = static_cast<const uint8_t *>(Wp);
     a.Y = Y;
     const int64_t nb = K / QK, T = (nb + 31) / 32;
-    a.row_bytes = T * Q4_0_TILE;
+    a.row_bytes = T * (wf == BQG_Q8_0 ? Q8_0_TILE : Q4_0_TILE);
     a.M = M;
     a.N = (int)N;
     a.K = (int)K;
@@ -425,14 +481,19 @@ int gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, in
         std::lock_guard<std::mutex> lk(mu);
         static bool attr = false;
         if (!attr) {
-            if (cudaFuncSetAttribute(gemm_q4_0_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-                cudaSuccess)
+            if (cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q4_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q8_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES) != cudaSuccess)
                 return BQG_ERR_CUDA;
             attr = true;
         }
     }
     const int grid = std::min(a.units, sms);
-    gemm_q4_0_bf16_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map, a);
+    if (wf == BQG_Q8_0)
+        gemm_bf16_kernel<BQG_Q8_0><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map, a);
+    else
+        gemm_bf16_kernel<BQG_Q4_0><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map, a);
     return cudaGetLastError() == cudaSuccess ? BQG_OK : BQG_ERR_CUDA;
 }
 

@@ -85,7 +85,8 @@ enum {
     BQG_OP_QKV_Q4_0_Q8_1 = 4,       /* N = Nq + 2*Nkv */
     BQG_OP_GATE_UP_Q4_0_Q8_1 = 5,   /* N = rows of each of gate and up */
     BQG_OP_GEMM_Q4_0_BF16 = 6,
-    BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1 = 7 /* gate+up SwiGLU with q8_1 output; N = rows of each */
+    BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1 = 7, /* gate+up SwiGLU with q8_1 output; N = rows of each */
+    BQG_OP_GEMM_Q8_0_BF16 = 8
 };
 
 /* ---- load time ------------------------------------------------------- */
@@ -209,11 +210,17 @@ int bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(const void *Wg, const void *Wu, const
                                            cudaStream_t stream);
 
 /* Prefill GEMM ("llama-3x-prompt-speed", "the tile"): each weight tile is
- * dequantized once to bf16 ((q-8)*d rounded to nearest-even bf16) in shared
- * memory and fed to the tensor cores with fp32 accumulation.
- * Wp: repacked q4_0 N x K; X: M x K bf16; Y: M x N fp32.
+ * dequantized once to bf16 ((q-8)*d rounded to nearest-even bf16) into the
+ * tensor memory the MMA reads and fed to the tensor cores with fp32
+ * accumulation.  Wp: repacked q4_0 N x K; X: M x K bf16; Y: M x N fp32.
  * M a positive multiple of 128, N a multiple of 128, K a multiple of 64. */
 int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
+                       void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The same prefill GEMM with q8_0 weights (the q8_0 tile of
+ * "llama-3x-prompt-speed", "the free 2x"): q * d rounded to nearest-even
+ * bf16.  Wp: repacked q8_0 N x K; other arguments as bqg_gemm_q4_0_bf16. */
+int bqg_gemm_q8_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
                        void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Debug export: the exact per-block integer dots of q4_0 x q8_1 for one

@@ -1,9 +1,9 @@
-"""Prefill GEMM (q4_0 weights x bf16 activations on the tensor cores) against
-the oracle, two ways:
+"""Prefill GEMM (q4_0 or q8_0 weights x bf16 activations on the tensor cores)
+against the oracle, two ways:
 
 * exactness of the tensor-core path: the oracle evaluated on the weights
   rounded to bf16 (the rounding the prefill page's tile applies before the
-  MMA: (q - 8) * d, one round-to-nearest-even), compared with an fp32
+  MMA: (q - 8) * d or q * d, one round-to-nearest-even), compared with an fp32
   accumulation bound, K * 2^-23 * sum_k |w_k x_k| + 1e-6;
 * the parity bound against the exact weights: |y - y_ref| <= 1e-3 *
   sum_k |w_k x_k| + 1e-6 for K >= 1024 (the full-size configuration
@@ -18,7 +18,7 @@ import torch
 import block_quantized_gemv_gb300 as bqg
 from block_quantized_gemv_gb300 import build as bqg_build
 from block_quantized_gemv_gb300 import synth
-from oracle import BF16, Q4_0
+from oracle import BF16, Q4_0, Q8_0
 
 from test_gpu_parity import gpu_repacked, make_weights, nan_like
 
@@ -35,13 +35,13 @@ def bf16_round(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
 
 
-def run_gemm(ora, M, N, K, seed, rows=None, cols=None):
-    _, canon = make_weights(ora, Q4_0, N, K, seed=seed)
-    Wp = gpu_repacked(Q4_0, canon, N, K)
+def run_gemm(ora, M, N, K, seed, rows=None, cols=None, fmt=Q4_0):
+    _, canon = make_weights(ora, fmt, N, K, seed=seed)
+    Wp = gpu_repacked(fmt, canon, N, K)
     xbits = synth.bf16_bits(synth.activations_f32(M, K, seed=seed + 1))
     X = synth.bf16_tensor(xbits)
     Y = nan_like((M, N))
-    bqg.gemm_q4_0_bf16(Wp, X, N, K, out=Y)
+    (bqg.gemm_q8_0_bf16 if fmt == Q8_0 else bqg.gemm_q4_0_bf16)(Wp, X, N, K, out=Y)
     torch.cuda.synchronize()
     assert bqg.last_device_error() == 0
     y = Y.cpu().double().numpy()
@@ -50,24 +50,25 @@ def run_gemm(ora, M, N, K, seed, rows=None, cols=None):
     sel_m = np.arange(M) if rows is None else rows
     ys = y[np.ix_(sel_m, sel_n)]
     # (1) exact tensor-core arithmetic on bf16-rounded weights
-    w_exact = ora.dequantize(Q4_0, canon.reshape(N, -1)[sel_n], len(sel_n), K)
+    w_exact = ora.dequantize(fmt, canon.reshape(N, -1)[sel_n], len(sel_n), K)
     wb = bf16_round(w_exact).view(torch.int16).numpy().view(np.uint16)
     Yb, Ab = ora.gemv(BF16, wb, BF16, xbits[sel_m], len(sel_m), len(sel_n), K, nthreads=16)
     err = np.abs(ys - Yb)
     bound = K * 2.0 ** -23 * Ab + 1e-6
     assert np.all(err <= bound), ("rounded-weight check", float(np.max(err / bound)))
     # (2) parity with the exact weights
-    Yr, Ar = ora.gemv(Q4_0, canon, BF16, xbits[sel_m], len(sel_m), N, K, rows=sel_n, nthreads=16)
+    Yr, Ar = ora.gemv(fmt, canon, BF16, xbits[sel_m], len(sel_m), N, K, rows=sel_n, nthreads=16)
     err = np.abs(ys - Yr)
     bound = (1e-3 if K >= 1024 else 1e-3 + 2.0 ** -9) * Ar + 1e-6
     assert np.all(err <= bound), ("parity", float(np.max(err / bound)))
     return Y, canon, X
 
 
+@pytest.mark.parametrize("fmt", [Q4_0, Q8_0])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (128, 256, 128), (256, 384, 1024), (384, 128, 4096),
                                    (128, 1024, 2048)])
-def test_gemm_small(ora, M, N, K):
-    run_gemm(ora, M, N, K, seed=M + N + K)
+def test_gemm_small(ora, M, N, K, fmt):
+    run_gemm(ora, M, N, K, seed=M + N + K, fmt=fmt)
 
 
 def test_gemm_matches_matmul_on_rounded_weights(ora):
@@ -89,6 +90,15 @@ def test_c5_prefill_m512_k4096_n14336(ora):
     run_gemm(ora, M, N, K, seed=77, rows=rows, cols=cols)
 
 
+@pytest.mark.slow
+def test_prefill_q8_0_m512_k4096_n14336(ora):
+    M, N, K = 512, 14336, 4096
+    rng = np.random.default_rng(1)
+    cols = np.unique(np.concatenate([rng.choice(N, 96, replace=False), [0, 127, 128, N - 1]]))
+    rows = np.unique(np.concatenate([rng.choice(M, 40, replace=False), [0, 127, 128, M - 1]]))
+    run_gemm(ora, M, N, K, seed=78, rows=rows, cols=cols, fmt=Q8_0)
+
+
 def test_gemm_rejects_bad_shapes():
     L = bqg.load()
     W = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
@@ -98,3 +108,4 @@ def test_gemm_rejects_bad_shapes():
     assert L.bqg_gemm_q4_0_bf16(W.data_ptr(), X.data_ptr(), Y.data_ptr(), 100, 128, 64, None, 0, s) == 2
     assert L.bqg_gemm_q4_0_bf16(W.data_ptr(), X.data_ptr(), Y.data_ptr(), 128, 100, 64, None, 0, s) == 2
     assert L.bqg_gemm_q4_0_bf16(W.data_ptr(), X.data_ptr(), Y.data_ptr(), 128, 128, 96, None, 0, s) == 2
+    assert L.bqg_gemm_q8_0_bf16(W.data_ptr(), X.data_ptr(), Y.data_ptr(), 128, 128, 96, None, 0, s) == 2
