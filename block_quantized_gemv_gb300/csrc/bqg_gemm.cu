@@ -4,11 +4,16 @@
 // tile is unpacked once and serves every activation row of the tile,
 // instead of being unpacked once per row.  Here the unit of work is 128
 // weight rows x 128 activation rows; per k-step of 64:
-//   * warps 1-8 (one q4_0 block of one weight row per thread) load the codes
-//     and scale eight k-steps ahead, dequantize (q - 8) * d exactly in fp32,
-//     round once to bf16 and store the 128 x 64 bf16 tile straight into
-//     tensor memory (tcgen05.st: lane = weight row, two k per column), where
-//     the MMA reads its A operand.  Shared memory then carries only the
+//   * warp 14, lane 0 stages the raw weight codes and scales of four k-steps
+//     at a time into shared memory with two-dimensional TMA copies (128 rows
+//     x 128 bytes of codes in the 128-byte swizzle, 128 rows x 16 bytes of
+//     scales), so the weight stream is coalesced;
+//   * warps 1-8 (one weight block of one weight row per thread) read their
+//     block's codes and scale from there (conflict-free thanks to the
+//     swizzle), dequantize q * d or (q - 8) * d exactly in fp32, round once to
+//     bf16 and store the 128 x 64 bf16 tile straight into tensor memory
+//     (tcgen05.st: lane = weight row, two k per column), where the MMA reads
+//     its A operand.  Shared memory then carries only the
 //     activation tiles: with A staged there too, its bandwidth (dequant
 //     writes, TMA writes and both MMA operands, 64 KiB per k-step) bounded
 //     the loop at twice the MMA time;
@@ -56,15 +61,27 @@ static_assert(A_COL0 + NSTAGE * A_COLS <= TMEM_COLS, "tensor memory budget");
 constexpr int DQ_WARPS = 8;                   // dequantizing warps (1..8)
 constexpr int EPI_WARP0 = 1 + DQ_WARPS;       // epilogue warps 9..12
 constexpr int TMA_WARP = EPI_WARP0 + 4;       // activation loads: warp 13
-constexpr int NUM_THREADS = (TMA_WARP + 1) * 32;
+constexpr int RAW_WARP = TMA_WARP + 1;        // raw weight codes: warp 14
+constexpr int NUM_THREADS = (RAW_WARP + 1) * 32;
+constexpr int RAW_STEPS = 4;                  // k-steps per raw group: 8 blocks = 128 code bytes (q4_0)
+constexpr int RAW_CODES = TM * 128;           // bytes of one 128-row x 128-byte code box
+constexpr int RAW_SCALES = TM * 16;           // bytes of one 128-row x 16-byte scale box
 
-// shared memory map (dynamic, 1024-byte aligned)
-constexpr int OFF_STAGES = 0;
-constexpr int OFF_BARS = NSTAGE * STAGE_BYTES;           // mbarriers
-constexpr int NBARS = 3 * NSTAGE + 4;                    // fullW, fullX, empty per stage; acc full/empty x2
-constexpr int OFF_TMEM_SLOT = OFF_BARS + NBARS * 8;
-constexpr int OFF_FLAG = OFF_TMEM_SLOT + 8;
-constexpr int SMEM_BYTES = OFF_FLAG + 8 + 1024;          // + slack for 1024-byte alignment
+// shared memory map (dynamic, 1024-byte aligned), per weight format
+template <int WF> struct GemmSmem {
+    static constexpr int CODE_BOXES = (WF == BQG_Q8_0) ? 2 : 1;   // q8_0: codes 0..15 and 16..31
+    static constexpr int NRAW = (WF == BQG_Q8_0) ? 2 : 3;         // raw groups in flight
+    static constexpr int RAW_GROUP = CODE_BOXES * RAW_CODES;
+    static constexpr int OFF_STAGES = 0;
+    static constexpr int OFF_RAW = NSTAGE * STAGE_BYTES;
+    static constexpr int OFF_SCALES = OFF_RAW + NRAW * RAW_GROUP;
+    static constexpr int OFF_BARS = OFF_SCALES + NRAW * RAW_SCALES;
+    // fullW, fullX, empty per stage; acc full/empty x2; raw full/empty per group
+    static constexpr int NBARS = 3 * NSTAGE + 4 + 2 * NRAW;
+    static constexpr int OFF_TMEM_SLOT = OFF_BARS + NBARS * 8;
+    static constexpr int OFF_FLAG = OFF_TMEM_SLOT + 8;
+    static constexpr int SMEM_BYTES = OFF_FLAG + 8 + 1024;       // + slack for 1024-byte alignment
+};
 
 // instruction descriptor, kind::f16: D fp32, A bf16, B bf16, both K-major, N, M
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TN >> 3) << 17) |
@@ -177,24 +194,19 @@ __device__ __forceinline__ uint4 dequant8_q8(uint32_t w0, uint32_t w1, float d)
                       pack_bf16x2(f[6], f[7]));
 }
 
-// One weight block's codes and scale as a dequantizing thread holds them, and
-// the repacked-tile addresses they come from (include/bqgemv.h).
+// A dequantizing thread's weight block, read from the raw group staged in
+// shared memory: `codes` is the group's 128 x 128-byte box (128-byte swizzle:
+// 16-byte chunk c of row r sits at chunk c ^ (r & 7)), `scales` the 128 x
+// 16-byte scale box, b8 the block within the group (0..7).
 template <int WF> struct BlockCodes;
 template <> struct BlockCodes<BQG_Q4_0> {
-    static constexpr int TILE = Q4_0_TILE;
-    static constexpr int PREFETCH = 8;       // k-steps of codes in flight per thread
-    uint4 c;
-    uint32_t s;
-    __device__ __forceinline__ void load(const uint8_t *tile, int s_)
-    {
-        c = ldg_v4(tile + 16 * s_);
-        s = __ldg(reinterpret_cast<const unsigned short *>(tile + 512 + 2 * s_));
-    }
-    __device__ __forceinline__ void clear() { c = make_uint4(0, 0, 0, 0); s = 0; }
+    static constexpr int TILE = Q4_0_TILE, SCALE_OFF = 512;
     // block elements 0..31 -> v[0..3] (8 each): low nibbles are 0..15, high 16..31
-    __device__ __forceinline__ void dequant(uint4 (&v)[4]) const
+    static __device__ __forceinline__ void dequant(const uint8_t *codes, const uint8_t *scales, int r, int b8,
+                                                   uint4 (&v)[4])
     {
-        const float d = half_bits_to_float(s);
+        const uint4 c = *reinterpret_cast<const uint4 *>(codes + r * 128 + ((b8 ^ (r & 7)) << 4));
+        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(scales + r * 16 + 2 * b8));
         v[0] = dequant8(c.x, c.y, 0, d);
         v[1] = dequant8(c.z, c.w, 0, d);
         v[2] = dequant8(c.x, c.y, 4, d);
@@ -202,20 +214,14 @@ template <> struct BlockCodes<BQG_Q4_0> {
     }
 };
 template <> struct BlockCodes<BQG_Q8_0> {
-    static constexpr int TILE = Q8_0_TILE;
-    static constexpr int PREFETCH = 4;
-    uint4 lo, hi;
-    uint32_t s;
-    __device__ __forceinline__ void load(const uint8_t *tile, int s_)
+    static constexpr int TILE = Q8_0_TILE, SCALE_OFF = 1024;
+    static __device__ __forceinline__ void dequant(const uint8_t *codes, const uint8_t *scales, int r, int b8,
+                                                   uint4 (&v)[4])
     {
-        lo = ldg_v4(tile + 16 * s_);
-        hi = ldg_v4(tile + 512 + 16 * s_);
-        s = __ldg(reinterpret_cast<const unsigned short *>(tile + 1024 + 2 * s_));
-    }
-    __device__ __forceinline__ void clear() { lo = hi = make_uint4(0, 0, 0, 0); s = 0; }
-    __device__ __forceinline__ void dequant(uint4 (&v)[4]) const
-    {
-        const float d = half_bits_to_float(s);
+        const int off = r * 128 + ((b8 ^ (r & 7)) << 4);
+        const uint4 lo = *reinterpret_cast<const uint4 *>(codes + off);             // codes 0..15
+        const uint4 hi = *reinterpret_cast<const uint4 *>(codes + RAW_CODES + off); // codes 16..31
+        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(scales + r * 16 + 2 * b8));
         v[0] = dequant8_q8(lo.x, lo.y, d);
         v[1] = dequant8_q8(lo.z, lo.w, d);
         v[2] = dequant8_q8(hi.x, hi.y, d);
@@ -234,8 +240,13 @@ struct GemmArgs {
 
 template <int WF>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_constant__ CUtensorMap xmap,
-                                                                        const GemmArgs a)
+                                                                   const __grid_constant__ CUtensorMap cmap,
+                                                                   const __grid_constant__ CUtensorMap smap,
+                                                                   const GemmArgs a)
 {
+    using SM = GemmSmem<WF>;
+    constexpr int OFF_STAGES = SM::OFF_STAGES, OFF_BARS = SM::OFF_BARS, OFF_TMEM_SLOT = SM::OFF_TMEM_SLOT;
+    constexpr int OFF_FLAG = SM::OFF_FLAG, NRAW = SM::NRAW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t sbase = smem_u32(smem);
@@ -245,6 +256,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
     auto bar_empty = [&](int s) { return bars + 8 * (2 * NSTAGE + s); };
     auto bar_accf = [&](int b) { return bars + 8 * (3 * NSTAGE + b); };
     auto bar_acce = [&](int b) { return bars + 8 * (3 * NSTAGE + 2 + b); };
+    auto bar_rawf = [&](int j) { return bars + 8 * (3 * NSTAGE + 4 + j); };
+    auto bar_rawe = [&](int j) { return bars + 8 * (3 * NSTAGE + 4 + NRAW + j); };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -259,6 +272,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
         for (int b = 0; b < 2; b++) {
             mbar_init(bar_accf(b), 1);      // tcgen05.commit after a unit's last k-step
             mbar_init(bar_acce(b), 4);      // one arrive per epilogue warp
+        }
+        for (int j = 0; j < NRAW; j++) {
+            mbar_init(bar_rawf(j), 1);      // the raw issuer's arrive + bytes
+            mbar_init(bar_rawe(j), DQ_WARPS);
         }
         *abort_flag = 0;
         mbar_fence_init();
@@ -321,6 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
         // ---------------- activation tiles (TMA) ----------------
         if (lane == 0) {
             int it = 0;
+            int issued = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
                 const int tm = u / a.tiles_n;                      // activation tile
@@ -333,9 +351,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
                     if (*abort_flag) { ok = false; break; }
                     mbar_arrive_expect_tx(bar_fullX(s), TILE_BYTES);
                     tma_load_2d(sbase + OFF_STAGES + s * STAGE_BYTES, &xmap, k * TK, tm * TN, bar_fullX(s));
+                    issued++;
                 }
                 it += nk;
             }
+            // do not leave while copies into shared memory are in flight (after an abort)
+            for (int q = (issued > NSTAGE ? issued - NSTAGE : 0); q < issued; q++)
+                mbar_wait_spin(bar_fullX(q % NSTAGE), (q / NSTAGE) & 1);
+        }
+        __syncwarp();
+    } else if (warp == RAW_WARP) {
+        // ---------------- raw weight codes and scales (TMA) ----------------
+        if (lane == 0) {
+            const int ng = (nk + RAW_STEPS - 1) / RAW_STEPS;   // raw groups per unit
+            int gi = 0;                                        // global group counter (ring position)
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                const int tn = u % a.tiles_n;
+                for (int g = 0; g < ng; g++, gi++) {
+                    const int j = gi % NRAW;
+                    if (gi >= NRAW && !mbar_wait_spin(bar_rawe(j), ((gi / NRAW) - 1) & 1)) {
+                        fail(); ok = false; break;
+                    }
+                    if (*abort_flag) { ok = false; break; }
+                    // blocks 8g .. 8g+7: tile t, slots s0 .. s0+7 (never past the row's last tile)
+                    const int t = g >> 2, s0 = 8 * (g & 3);
+                    const int x = t * BlockCodes<WF>::TILE + 16 * s0;
+                    const uint32_t dst = sbase + SM::OFF_RAW + j * SM::RAW_GROUP;
+                    mbar_arrive_expect_tx(bar_rawf(j), SM::RAW_GROUP + RAW_SCALES);
+                    tma_load_2d(dst, &cmap, x, tn * TM, bar_rawf(j));
+                    if (SM::CODE_BOXES == 2) tma_load_2d(dst + RAW_CODES, &cmap, x + 512, tn * TM, bar_rawf(j));
+                    tma_load_2d(sbase + SM::OFF_SCALES + j * RAW_SCALES, &smap,
+                                t * BlockCodes<WF>::TILE + BlockCodes<WF>::SCALE_OFF + 2 * s0, tn * TM, bar_rawf(j));
+                }
+            }
+            // do not leave while copies into shared memory are in flight (after an abort)
+            for (int q = (gi > NRAW ? gi - NRAW : 0); q < gi; q++) mbar_wait_spin(bar_rawf(q % NRAW), (q / NRAW) & 1);
         }
         __syncwarp();
     } else if (warp <= DQ_WARPS) {
@@ -346,46 +397,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
         const int r = quarter * 32 + lane;                   // weight row in the unit
         const int h = (warp - 1) >> 2;                       // which of the step's two blocks
         const uint32_t arow = tmem + ((uint32_t)(quarter * 32) << 16) + A_COL0 + h * (A_COLS / 2);
-        int it = 0;
+        int it = 0;       // global k-step counter (A slot ring)
+        int gi = 0;       // global raw-group counter (raw ring)
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            const int tn = u % a.tiles_n;
-            const uint8_t *row = a.W + (int64_t)(tn * TM + r) * a.row_bytes;
-            // block 2k + h of this row: its codes and fp16 scale
-            auto load = [&](int k, BlockCodes<WF> &c) {
-                if (k >= nk) return;
-                const int blk = 2 * k + h;
-                c.load(row + (int64_t)(blk >> 5) * BlockCodes<WF>::TILE, blk & 31);
-            };
-            // ring of PREFETCH k-steps of codes and scales in registers; the loop
-            // is unrolled by PREFETCH so each slot is reloaded right after use
-            // and never moved while its load is in flight
-            constexpr int PREFETCH = BlockCodes<WF>::PREFETCH;
-            BlockCodes<WF> cr[PREFETCH];
-#pragma unroll
-            for (int i = 0; i < PREFETCH; i++) {
-                cr[i].clear();
-                load(i, cr[i]);
-            }
-            for (int k0 = 0; k0 < nk && ok; k0 += PREFETCH) {
-#pragma unroll
-                for (int i = 0; i < PREFETCH; i++) {
-                    const int k = k0 + i;
-                    if (k >= nk) break;
-                    const int step = it + k;
-                    const int s = step % NSTAGE;
-                    // the whole warp takes the same branch (tcgen05.st is warp-wide)
-                    const bool free_slot = step < NSTAGE || mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1);
-                    if (!__all_sync(0xffffffffu, free_slot)) { fail(); ok = false; break; }
-                    if (*abort_flag) { ok = false; break; }
-                    // block h covers k 32h .. 32h+31 of the step: 16 columns of the slot
-                    uint4 v[4];
-                    cr[i].dequant(v);
-                    load(k + PREFETCH, cr[i]);
-                    tmem_st16(arow + s * A_COLS, v);
-                    tc_fence_before();                             // tensor-memory writes -> the MMA thread
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_fullW(s));
+            for (int k = 0; k < nk && ok; k++) {
+                const int kq = k % RAW_STEPS;
+                const int j = gi % NRAW;
+                if (kq == 0) {
+                    const bool raw_ready = mbar_wait_spin(bar_rawf(j), (gi / NRAW) & 1);
+                    if (!__all_sync(0xffffffffu, raw_ready)) { fail(); ok = false; break; }
+                }
+                const int step = it + k;
+                const int s = step % NSTAGE;
+                // the whole warp takes the same branch (tcgen05.st is warp-wide)
+                const bool free_slot = step < NSTAGE || mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1);
+                if (!__all_sync(0xffffffffu, free_slot)) { fail(); ok = false; break; }
+                if (*abort_flag) { ok = false; break; }
+                // block h of the step is block 2 kq + h of the raw group: 16 columns of the A slot
+                uint4 v[4];
+                BlockCodes<WF>::dequant(smem + SM::OFF_RAW + j * SM::RAW_GROUP, smem + SM::OFF_SCALES + j * RAW_SCALES,
+                                        r, 2 * kq + h, v);
+                tmem_st16(arow + s * A_COLS, v);
+                tc_fence_before();                             // tensor-memory writes -> the MMA thread
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_fullW(s));
+                if (kq == RAW_STEPS - 1 || k == nk - 1) {      // done with this raw group
+                    if (lane == 0) mbar_arrive(bar_rawe(j));
+                    gi++;
                 }
             }
             it += nk;
@@ -467,11 +506,25 @@ int gemm_bf16(int wf, const void *Wp, const void *X, float *Y, int M, int64_t N,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return BQG_ERR_CUDA;
+    // the repacked weights as a 2-D byte array (row_bytes x N): 128-row boxes
+    // of 128 code bytes (128-byte swizzle) and of 16 scale bytes
+    const int64_t nb = K / QK, T = (nb + 31) / 32;
+    const int64_t row_bytes = T * (wf == BQG_Q8_0 ? Q8_0_TILE : Q4_0_TILE);
+    CUtensorMap cmap, smap;
+    const cuuint64_t wdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)N};
+    const cuuint64_t wstride[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t cbox[2] = {128, TM}, sbox[2] = {16, TM};
+    if (enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Wp), wdim, wstride, cbox, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(Wp), wdim, wstride, sbox, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return BQG_ERR_CUDA;
     GemmArgs a;
     a.W = static_cast<const uint8_t *>(Wp);
     a.Y = Y;
-    const int64_t nb = K / QK, T = (nb + 31) / 32;
-    a.row_bytes = T * (wf == BQG_Q8_0 ? Q8_0_TILE : Q4_0_TILE);
+    a.row_bytes = row_bytes;
     a.M = M;
     a.N = (int)N;
     a.K = (int)K;
@@ -482,18 +535,18 @@ int gemm_bf16(int wf, const void *Wp, const void *X, float *Y, int M, int64_t N,
         static bool attr = false;
         if (!attr) {
             if (cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q4_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess ||
+                                     GemmSmem<BQG_Q4_0>::SMEM_BYTES) != cudaSuccess ||
                 cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q8_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES) != cudaSuccess)
+                                     GemmSmem<BQG_Q8_0>::SMEM_BYTES) != cudaSuccess)
                 return BQG_ERR_CUDA;
             attr = true;
         }
     }
     const int grid = std::min(a.units, sms);
     if (wf == BQG_Q8_0)
-        gemm_bf16_kernel<BQG_Q8_0><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map, a);
+        gemm_bf16_kernel<BQG_Q8_0><<<grid, NUM_THREADS, GemmSmem<BQG_Q8_0>::SMEM_BYTES, stream>>>(map, cmap, smap, a);
     else
-        gemm_bf16_kernel<BQG_Q4_0><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map, a);
+        gemm_bf16_kernel<BQG_Q4_0><<<grid, NUM_THREADS, GemmSmem<BQG_Q4_0>::SMEM_BYTES, stream>>>(map, cmap, smap, a);
     return cudaGetLastError() == cudaSuccess ? BQG_OK : BQG_ERR_CUDA;
 }
 
