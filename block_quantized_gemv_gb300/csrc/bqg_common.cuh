@@ -223,6 +223,17 @@ __device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 // (a0 + c, a1 + c) with one rounding each
+// (a0, a1) *= (c, c), one packed instruction
+__device__ __forceinline__ void fmul2(float &a0, float &a1, float c)
+{
+    asm("{\n\t.reg .b64 ra, rc;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rc, {%2, %2};\n\t"
+        "mul.rn.f32x2 ra, ra, rc;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(c));
+}
 __device__ __forceinline__ void fadd2(float &a0, float &a1, float c)
 {
     asm("{\n\t.reg .b64 ra, rc;\n\t"

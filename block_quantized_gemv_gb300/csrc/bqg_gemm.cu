@@ -49,9 +49,11 @@ namespace {
 
 constexpr int TM = 128;         // weight rows per unit (MMA M)
 constexpr int TN = 128;         // activation rows per unit (MMA N)
-constexpr int TK = 64;          // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int NSTAGE = 8;
-constexpr int TILE_BYTES = TN * TK * 2;       // 16 KiB activation tile
+constexpr int TK = 128;         // K per stage: two 128-byte swizzle atoms of bf16
+constexpr int XATOM = 64;       // K of one swizzle atom (one TMA box)
+constexpr int ATOM_BYTES = TN * XATOM * 2;    // 16 KiB
+constexpr int NSTAGE = 4;
+constexpr int TILE_BYTES = TN * TK * 2;       // 32 KiB activation tile
 constexpr int STAGE_BYTES = TILE_BYTES;
 constexpr int ACC_COLS = TN;                  // fp32 columns per accumulator
 constexpr int A_COL0 = 2 * ACC_COLS;          // first column of the A slots
@@ -63,7 +65,7 @@ constexpr int EPI_WARP0 = 1 + DQ_WARPS;       // epilogue warps 9..12
 constexpr int TMA_WARP = EPI_WARP0 + 4;       // activation loads: warp 13
 constexpr int RAW_WARP = TMA_WARP + 1;        // raw weight codes: warp 14
 constexpr int NUM_THREADS = (RAW_WARP + 1) * 32;
-constexpr int RAW_STEPS = 4;                  // k-steps per raw group: 8 blocks = 128 code bytes (q4_0)
+constexpr int RAW_STEPS = 2;                  // stages per raw group: 8 blocks = 128 code bytes (q4_0)
 constexpr int RAW_CODES = TM * 128;           // bytes of one 128-row x 128-byte code box
 constexpr int RAW_SCALES = TM * 16;           // bytes of one 128-row x 16-byte scale box
 
@@ -119,8 +121,8 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
 }
 
 // 32 lanes x 16 columns of 32-bit words into tensor memory (this warp's lane
-// quarter), then wait until they are written
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4])
+// quarter); tcgen05.wait::st makes them complete
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint4 (&v)[4])
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
                  "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
@@ -128,7 +130,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4])
                    "r"(v[1].z), "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x),
                    "r"(v[3].y), "r"(v[3].z), "r"(v[3].w)
                  : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -175,7 +176,10 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, int shift, f
     float f[8] = {byte_plus_2p23<0>(a), byte_plus_2p23<1>(a), byte_plus_2p23<2>(a), byte_plus_2p23<3>(a),
                   byte_plus_2p23<0>(b), byte_plus_2p23<1>(b), byte_plus_2p23<2>(b), byte_plus_2p23<3>(b)};
 #pragma unroll
-    for (int i = 0; i < 8; i++) f[i] = (f[i] - OFF) * d;     // exact: 4-bit integer times an fp16 value
+    for (int i = 0; i < 8; i += 2) {          // exact: 4-bit integer times an fp16 value
+        fadd2(f[i], f[i + 1], -OFF);
+        fmul2(f[i], f[i + 1], d);
+    }
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                       pack_bf16x2(f[6], f[7]));
 }
@@ -189,7 +193,10 @@ __device__ __forceinline__ uint4 dequant8_q8(uint32_t w0, uint32_t w1, float d)
     float f[8] = {byte_plus_2p23<0>(a), byte_plus_2p23<1>(a), byte_plus_2p23<2>(a), byte_plus_2p23<3>(a),
                   byte_plus_2p23<0>(b), byte_plus_2p23<1>(b), byte_plus_2p23<2>(b), byte_plus_2p23<3>(b)};
 #pragma unroll
-    for (int i = 0; i < 8; i++) f[i] = (f[i] - OFF) * d;     // exact: 8-bit integer times an fp16 value
+    for (int i = 0; i < 8; i += 2) {          // exact: 8-bit integer times an fp16 value
+        fadd2(f[i], f[i + 1], -OFF);
+        fmul2(f[i], f[i + 1], d);
+    }
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                       pack_bf16x2(f[6], f[7]));
 }
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nk = a.K / TK;
+    const int nk = (a.K + TK - 1) / TK;              // stages per unit (a last one may hold K = 64)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; s++) {
@@ -322,9 +329,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
                     tc_fence_after();
                     const uint32_t aw = tmem + A_COL0 + s * A_COLS;                 // weights: MMA A (M = 128 rows)
                     const uint32_t bx = sbase + OFF_STAGES + s * STAGE_BYTES;       // activations: MMA B (N = 128)
+                    // a last stage of K = 64 (K % 128 == 64) holds one atom
+                    const int nkk = (k == nk - 1 && (a.K % TK) != 0) ? XATOM / 16 : TK / 16;
 #pragma unroll
-                    for (int kk = 0; kk < TK / 16; kk++)
-                        umma_bf16_ts(dacc, aw + kk * 8, sw128_desc(bx + kk * 32), (k > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < TK / 16; kk++) {
+                        if (kk >= nkk) break;
+                        umma_bf16_ts(dacc, aw + kk * 8, sw128_desc(bx + (kk >> 2) * ATOM_BYTES + (kk & 3) * 32),
+                                     (k > 0 || kk > 0) ? 1u : 0u);
+                    }
                     umma_commit(bar_empty(s));               // stage s is free when these MMAs finish
                 }
                 if (ok) umma_commit(bar_accf(b));            // the unit's accumulator is complete
@@ -349,8 +361,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
                         fail(); ok = false; break;
                     }
                     if (*abort_flag) { ok = false; break; }
-                    mbar_arrive_expect_tx(bar_fullX(s), TILE_BYTES);
+                    const bool half = (k == nk - 1) && (a.K % TK) != 0;
+                    mbar_arrive_expect_tx(bar_fullX(s), half ? ATOM_BYTES : TILE_BYTES);
                     tma_load_2d(sbase + OFF_STAGES + s * STAGE_BYTES, &xmap, k * TK, tm * TN, bar_fullX(s));
+                    if (!half)
+                        tma_load_2d(sbase + OFF_STAGES + s * STAGE_BYTES + ATOM_BYTES, &xmap, k * TK + XATOM, tm * TN,
+                                    bar_fullX(s));
                     issued++;
                 }
                 it += nk;
@@ -392,10 +408,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
     } else if (warp <= DQ_WARPS) {
         // ---------------- weight dequantization (warps 1-8) ----------------
         // a warp may only reach its lane quarter of tensor memory: warps 1-4 and
-        // 5-8 each cover quarters 1, 2, 3, 0, for the step's first and second block
+        // 5-8 each cover quarters 1, 2, 3, 0, for the stage's blocks 0-1 and 2-3
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;                   // weight row in the unit
-        const int h = (warp - 1) >> 2;                       // which of the step's two blocks
+        const int h = (warp - 1) >> 2;                       // which pair of the stage's four blocks
         const uint32_t arow = tmem + ((uint32_t)(quarter * 32) << 16) + A_COL0 + h * (A_COLS / 2);
         int it = 0;       // global k-step counter (A slot ring)
         int gi = 0;       // global raw-group counter (raw ring)
@@ -414,11 +430,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
                 const bool free_slot = step < NSTAGE || mbar_wait_spin(bar_empty(s), ((step / NSTAGE) - 1) & 1);
                 if (!__all_sync(0xffffffffu, free_slot)) { fail(); ok = false; break; }
                 if (*abort_flag) { ok = false; break; }
-                // block h of the step is block 2 kq + h of the raw group: 16 columns of the A slot
-                uint4 v[4];
-                BlockCodes<WF>::dequant(smem + SM::OFF_RAW + j * SM::RAW_GROUP, smem + SM::OFF_SCALES + j * RAW_SCALES,
-                                        r, 2 * kq + h, v);
-                tmem_st16(arow + s * A_COLS, v);
+                // blocks 2h, 2h+1 of the stage are blocks 4 kq + 2h (+1) of the raw group:
+                // 32 columns of the A slot (a last half stage has blocks 0-1 only)
+                const bool half = (k == nk - 1) && (a.K % TK) != 0;
+                if (!(half && h == 1)) {
+                    const uint8_t *codes = smem + SM::OFF_RAW + j * SM::RAW_GROUP;
+                    const uint8_t *scales = smem + SM::OFF_SCALES + j * RAW_SCALES;
+                    uint4 v[4];
+                    BlockCodes<WF>::dequant(codes, scales, r, 4 * kq + 2 * h, v);
+                    tmem_st16_nowait(arow + s * A_COLS, v);
+                    BlockCodes<WF>::dequant(codes, scales, r, 4 * kq + 2 * h + 1, v);
+                    tmem_st16_nowait(arow + s * A_COLS + 16, v);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
                 tc_fence_before();                             // tensor-memory writes -> the MMA thread
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_fullW(s));
@@ -500,7 +524,7 @@ int gemm_bf16(int wf, const void *Wp, const void *X, float *Y, int M, int64_t N,
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {TK, TN};
+    const cuuint32_t box[2] = {XATOM, TN};
     const cuuint32_t estride[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(X), gdim, gstride, box, estride,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
