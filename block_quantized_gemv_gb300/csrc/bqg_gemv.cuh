@@ -93,13 +93,6 @@ static __device__ int g_gemv_error;
 // the block encodes it from L2 and re-arms the counter for the next call.
 // Nothing waits on another CTA.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool swiglu_store(const GemvParams &p, int m, int64_t o, float h)
-{
-    p.Y[0][(int64_t)m * p.rows[0] + o] = h;
-    if (!p.hq) return false;
-    __threadfence();
-    return atomicAdd(p.cnt + (int64_t)m * (p.rows[0] / 32) + o / 32, 1) == 31;
-}
 // warp-wide: encode block b of activation row m
 __device__ __forceinline__ void swiglu_encode_block_warp(const GemvParams &p, int m, int64_t b, int lane)
 {
@@ -108,33 +101,6 @@ __device__ __forceinline__ void swiglu_encode_block_warp(const GemvParams &p, in
     const float v = __ldcg(p.Y[0] + (int64_t)m * p.rows[0] + b * 32 + lane);
     q8_1_encode_warp(v, lane, p.hq + blk * Q8_1_BYTES);
     if (lane == 0) p.cnt[blk] = 0;
-}
-// one thread: the same encoding, element by element
-__device__ __forceinline__ void swiglu_encode_block_thread(const GemvParams &p, int m, int64_t b)
-{
-    __threadfence();
-    const int64_t blk = (int64_t)m * (p.rows[0] / 32) + b;
-    const float *h = p.Y[0] + (int64_t)m * p.rows[0] + b * 32;
-    float v[32];
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; i++) {
-        v[i] = __ldcg(h + i);
-        amax = fmaxf(amax, fabsf(v[i]));
-    }
-    const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
-    const float d = __half2float(dh);
-    uint8_t *out = p.hq + blk * Q8_1_BYTES;
-    int sum = 0;
-#pragma unroll
-    for (int i = 0; i < 32; i++) {
-        const int q = q8_code(v[i], d);
-        sum += q;
-        out[4 + i] = (uint8_t)(int8_t)q;
-    }
-    const __half sh = __float2half_rn(d * (float)sum);
-    *reinterpret_cast<uint32_t *>(out) = (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(sh) << 16);
-    p.cnt[blk] = 0;
 }
 
 // Virtual row -> (matrix, row in matrix)
@@ -407,6 +373,33 @@ __device__ __forceinline__ void named_barrier(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// The SwiGLU q8_1 output of a CTA, once its fp32 outputs [o0, o1) of every
+// activation row are stored by the `nwarps` warps that meet at barrier
+// `bar`: one fence and barrier, then per (block, row) one counted arrival
+// carrying the number of outputs this CTA gave the block.  A block wholly
+// inside the range is complete at once and skips the counter.
+__device__ __forceinline__ void swiglu_q8_1_finish(const GemvParams &p, int M, int64_t o0, int64_t o1, int bar,
+                                                   int warp, int nwarps, int lane)
+{
+    __threadfence();
+    named_barrier(bar, nwarps * 32);
+    if (o1 <= o0) return;
+    const int64_t b0 = o0 / 32;
+    const int nbm = (int)((o1 - 1) / 32 - b0 + 1) * M;
+    for (int i = warp; i < nbm; i += nwarps) {
+        const int64_t b = b0 + i / M;
+        const int m = i - (i / M) * M;
+        const int c = (int)(min(o1, 32 * (b + 1)) - max(o0, 32 * b));
+        bool last = true;
+        if (c < 32) {
+            int prev = 0;
+            if (lane == 0) prev = atomicAdd(p.cnt + (int64_t)m * (p.rows[0] / 32) + b, c);
+            last = (__shfl_sync(0xffffffffu, prev, 0) + c == 32);
+        }
+        if (last) swiglu_encode_block_warp(p, m, b, lane);
+    }
+}
+
 // rows each group takes from a stage (per pass); V = RPS * M values per warp reduction
 template <int M> struct RowsPerStage { static constexpr int value = (M == 8) ? 1 : 4 / M; };
 
@@ -641,7 +634,7 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
                         us += part[((2 * pr + 1) * WPG + w) * M + m];
                     }
                     const int64_t o = (win0 >> 1) + pr;
-                    if (swiglu_store(p, m, o, silu(gs) * us)) swiglu_encode_block_thread(p, m, o / 32);
+                    p.Y[0][(int64_t)m * p.rows[0] + o] = silu(gs) * us;
                 }
             } else {
                 for (int t = tid; t < nrw * M; t += ncons) {
@@ -663,6 +656,7 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
             win0 += WIN;
         }
     }
+    if (p.epi == EPI_SWIGLU && p.hq) swiglu_q8_1_finish(p, M, v0 >> 1, v1 >> 1, 1, tid >> 5, ncons >> 5, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1099,11 +1093,8 @@ __global__ void __launch_bounds__(384, 2) gemv_lpr_kernel(const GemvParams p)
                 const int64_t v = staged_vrow(p, vb, RL, k);
                 const bool valid = ok && v < v1;
 #pragma unroll
-                for (int m = 0; m < M; m++) {
-                    bool last = false;
-                    if (lane == 0 && valid) last = swiglu_store(p, m, v >> 1, silu(tot[k][m]) * tot[RL / 2 + k][m]);
-                    if (__shfl_sync(0xffffffffu, (int)last, 0)) swiglu_encode_block_warp(p, m, (v >> 1) / 32, lane);
-                }
+                for (int m = 0; m < M; m++)
+                    if (lane == 0 && valid) p.Y[0][(int64_t)m * p.rows[0] + (v >> 1)] = silu(tot[k][m]) * tot[RL / 2 + k][m];
             }
             continue;
         }
@@ -1132,6 +1123,7 @@ __global__ void __launch_bounds__(384, 2) gemv_lpr_kernel(const GemvParams p)
             mbar_wait_bounded(wbar + 8 * (t % D), (uint32_t)((t / D) & 1));
     }
     if (tid == 0 && !xok) mbar_wait_bounded(xbar, 0);
+    if (swiglu && p.hq) swiglu_q8_1_finish(p, M, v0 >> 1, v1 >> 1, 0, warp, NW, lane);
 }
 
 template <int WF, int XF, int M, int RL>

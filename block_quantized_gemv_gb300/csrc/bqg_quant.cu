@@ -11,6 +11,8 @@
 // megakernel": 18-byte q4_0 blocks; "rx-6700xt-llama2-decode": Q8_1
 // activations of the integer-dot matvec).  Divisions use __fdiv_rn so the
 // result does not depend on fast-math flags.
+#include <algorithm>
+
 #include "bqg_gemv.cuh"
 
 namespace bqg {
@@ -38,43 +40,159 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void *__restri
     q8_1_encode_warp(load_act(x, x_f32, m * K + b * QK + lane), lane, xq + blk * Q8_1_BYTES);
 }
 
-// Fused RMSNorm -> q8_1, one CTA per activation row ("MI50 megakernel",
-// hypothesis ledger: neighbouring steps fused into one dispatch; the Q8_1
-// activation of "rx-6700xt-llama2-decode").  s = sum x^2 is accumulated in
-// fp64, which is exact for bf16 inputs whatever the order (each square has
-// 16 significant bits), r = fp32(1 / sqrt(s / K + eps)) in fp64, then
-// y = fp32(fp32(x * r) * gamma) goes through the q8_1 encoder, one warp per
-// block.
-__global__ void __launch_bounds__(256) rmsnorm_q8_1_kernel(const void *__restrict__ x, int x_f32,
+// Knuth's TwoSum: s + e == a + b exactly (round-to-nearest, no contraction).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Sum of squares as an unevaluated pair hi + lo of fp32 values, plus an fp64
+// part for magnitudes whose square or its rounding error would leave the
+// normal fp32 range.  Each square is exact as p + e (e = fma(v, v, -p); zero
+// for bf16 inputs), hi takes the exact TwoSum of p, lo the rest.
+struct SumSq {
+    float hi = 0.f, lo = 0.f;
+    double wide = 0.0;
+    __device__ __forceinline__ void add(float v)
+    {
+        const uint32_t ex = (__float_as_uint(v) >> 23) & 0xFFu;
+        if (ex - 77u <= 176u - 77u) {                 // 2^-50 <= |v| < 2^50
+            const float p = __fmul_rn(v, v);
+            const float ep = fmaf(v, v, -p);
+            float t;
+            two_sum(hi, p, hi, t);
+            lo = __fadd_rn(lo, __fadd_rn(t, ep));
+        } else if (v != 0.f) {
+            wide = fma((double)v, (double)v, wide);   // exact square in fp64
+        }
+    }
+    __device__ __forceinline__ void merge(float ohi, float olo)
+    {
+        float t;
+        two_sum(hi, ohi, hi, t);
+        lo = __fadd_rn(lo, __fadd_rn(olo, t));
+    }
+};
+
+// r = 1 / sqrt(s / K + eps) rounded once to fp32, from s = sh + sl, without
+// fp64: u = s / K + eps is formed as an fp32 pair (q1 = RN(sh / K), whose
+// remainder sh - q1 K an fma gives exactly), then y = rsqrtf(u) is refined by
+// one Newton step for u^-1/2 with its second-order term,
+// y (1 + d/2 + 3 d^2 / 8), d = 1 - u y^2, the products split exactly by fma.
+// Before the last rounding the value is within about 2^-44 of the exact one.
+__device__ __forceinline__ float rms_recip_pair(float sh, float sl, float Kf, float eps)
+{
+    const float q1 = __fdiv_rn(sh, Kf);
+    const float rem = fmaf(-q1, Kf, sh);
+    const float q2 = __fdiv_rn(__fadd_rn(rem, sl), Kf);
+    float uh, ul;
+    two_sum(q1, eps, uh, ul);
+    ul = __fadd_rn(ul, q2);
+    const float t = __fadd_rn(uh, ul);                 // renormalise (|uh| >= |ul|)
+    ul = __fsub_rn(ul, __fsub_rn(t, uh));
+    uh = t;
+    const float y = rsqrtf(uh);
+    const float p = __fmul_rn(y, y), pe = fmaf(y, y, -p);
+    const float wh = __fmul_rn(uh, p), we = fmaf(uh, p, -wh);
+    const float d = __fsub_rn(__fsub_rn(__fsub_rn(1.0f, wh), we), fmaf(uh, pe, __fmul_rn(ul, p)));
+    return __fadd_rn(y, __fmul_rn(y, __fmul_rn(d, fmaf(0.375f, d, 0.5f))));
+}
+
+// Fused RMSNorm -> q8_1 ("MI50 megakernel", hypothesis ledger: neighbouring
+// steps fused into one dispatch; the Q8_1 activation of "rx-6700xt-llama2-
+// decode").  Grid: blockIdx.y = activation row, blockIdx.x = a slice of its
+// blocks.  Every CTA of a row computes s = sum x^2 (the same value in each, in
+// the same order) to about 2^-44 relative: squares exact, accumulated as
+// fp32 pairs with error-free sums.  Then r = 1 / sqrt(s / K + eps) to about
+// 2^-44 relative, rounded once to fp32 (in fp64 when an input or s leaves the
+// range the pair arithmetic covers), and its warps encode
+// y = fp32(fp32(x * r) * gamma) of their blocks with the q8_1 encoder.
+// fp64 arithmetic is kept off the common path: its rate, and the issue time
+// of one warp's fp64 instruction, are a small fraction of fp32's on this part.
+__global__ void __launch_bounds__(256) rmsnorm_q8_1_kernel(const void *__restrict__ x, int x_f32, int vec,
                                                            const float *__restrict__ gamma, float eps,
                                                            uint8_t *__restrict__ xq, int nb, int64_t K)
 {
-    __shared__ double part[8];
+    __shared__ float part_hi[8], part_lo[8];
+    __shared__ double part_w[8];
     __shared__ float s_r;
     pdl_wait();
     pdl_launch_dependents();
-    const int64_t m = blockIdx.x;
+    const int64_t m = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    double s = 0.0;
-    for (int64_t k = tid; k < K; k += 256) {
-        const double v = (double)load_act(x, x_f32, m * K + k);
-        s += v * v;                                   // exact square (<= 48 bits)
+    // this warp's first block, loaded beside the sum so that its L2 trip overlaps
+    const int bfirst = blockIdx.x * 8 + warp;
+    float x0 = 0.f, g0 = 1.f;
+    if (bfirst < nb) {
+        const int64_t k = (int64_t)bfirst * QK + lane;
+        x0 = load_act(x, x_f32, m * K + k);
+        if (gamma) g0 = gamma[k];
+    }
+    SumSq acc;
+    if (vec && x_f32) {
+        const float4 *row = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + m * K);
+        for (int64_t i = tid; i < K / 4; i += 256) {
+            const float4 q = row[i];
+            acc.add(q.x); acc.add(q.y); acc.add(q.z); acc.add(q.w);
+        }
+    } else if (vec) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(x) + m * K);
+        for (int64_t i = tid; i < K / 8; i += 256) {
+            const uint4 q = row[i];
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                acc.add(__uint_as_float(w[j] << 16));
+                acc.add(__uint_as_float(w[j] & 0xFFFF0000u));
+            }
+        }
+    } else {
+        for (int64_t k = tid; k < K; k += 256) acc.add(load_act(x, x_f32, m * K + k));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) part[warp] = s;
+    for (int o = 16; o > 0; o >>= 1)
+        acc.merge(__shfl_xor_sync(0xffffffffu, acc.hi, o), __shfl_xor_sync(0xffffffffu, acc.lo, o));
+    if (__any_sync(0xffffffffu, acc.wide != 0.0)) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc.wide += __shfl_xor_sync(0xffffffffu, acc.wide, o);
+    }
+    if (lane == 0) {
+        part_hi[warp] = acc.hi;
+        part_lo[warp] = acc.lo;
+        part_w[warp] = acc.wide;
+    }
     __syncthreads();
-    if (tid == 0) {
-        double t = 0.0;
-        for (int w = 0; w < 8; w++) t += part[w];
-        s_r = (float)(1.0 / sqrt(t / (double)K + (double)eps));
+    if (warp == 0) {
+        SumSq tot;
+        if (lane < 8) {
+            tot.hi = part_hi[lane];
+            tot.lo = part_lo[lane];
+            tot.wide = part_w[lane];
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1)
+            tot.merge(__shfl_xor_sync(0xffffffffu, tot.hi, o), __shfl_xor_sync(0xffffffffu, tot.lo, o));
+        const bool wide = __any_sync(0xffffffffu, tot.wide != 0.0);
+        if (lane == 0) {
+            // pair path: s and s / K well inside the normal fp32 range
+            if (!wide && tot.hi >= 0x1p-60f && tot.hi <= 0x1p100f && eps >= 0.f && K < (1 << 24)) {
+                s_r = rms_recip_pair(tot.hi, tot.lo, (float)K, eps);
+            } else {
+                double t = 0.0;
+                for (int w = 0; w < 8; w++) t += ((double)part_hi[w] + (double)part_lo[w]) + part_w[w];
+                s_r = (float)(1.0 / sqrt(t / (double)K + (double)eps));
+            }
+        }
     }
     __syncthreads();
     const float r = s_r;
-    for (int b = warp; b < nb; b += 8) {
+    for (int b = bfirst; b < nb; b += gridDim.x * 8) {
         const int64_t k = (int64_t)b * QK + lane;
-        float y = __fmul_rn(load_act(x, x_f32, m * K + k), r);
-        if (gamma) y = __fmul_rn(y, gamma[k]);
+        const bool first = (b == bfirst);
+        float y = __fmul_rn(first ? x0 : load_act(x, x_f32, m * K + k), r);
+        if (gamma) y = __fmul_rn(y, first ? g0 : gamma[k]);
         q8_1_encode_warp(y, lane, xq + (m * nb + b) * Q8_1_BYTES);
     }
 }
@@ -205,7 +323,8 @@ cudaError_t launch_rmsnorm_q8_1(const void *x, int x_f32, const float *gamma, fl
                                cudaStream_t s, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)M);
+    const int nb = (int)(K / QK);
+    cfg.gridDim = dim3((unsigned)std::min((nb + 7) / 8, 64), (unsigned)M);   // up to 64 CTAs per row
     cfg.blockDim = dim3(256);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -213,7 +332,8 @@ cudaError_t launch_rmsnorm_q8_1(const void *x, int x_f32, const float *gamma, fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, rmsnorm_q8_1_kernel, x, x_f32, gamma, eps, (uint8_t *)xq, (int)(K / QK), K);
+    const int vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;   // rows are then 16-byte aligned too
+    return cudaLaunchKernelEx(&cfg, rmsnorm_q8_1_kernel, x, x_f32, vec, gamma, eps, (uint8_t *)xq, (int)(K / QK), K);
 }
 
 cudaError_t launch_quantize_weights(int fmt, const float *W, void *dst, int64_t N, int64_t K, cudaStream_t s)
