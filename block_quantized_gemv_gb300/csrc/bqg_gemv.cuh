@@ -980,7 +980,17 @@ __global__ void __launch_bounds__(384, 2) gemv_lpr_kernel(const GemvParams p)
     const int units = (WF == W_BF16) ? p.nc : p.nb;
 
     // stage t of this warp: block warp + NW * (t / npc), piece t % npc
+    // one matrix, whole rows: a stage is RL consecutive rows, one copy
+    const bool simple = (p.nmat == 1 && npc == 1 && cbeg == 0 && cend == p.nc);
+    const uint8_t *wrow0 = p.W[0] + v0 * p.row_bytes;
     auto issue = [&](int t, int slot) {
+        if (simple) {
+            const int r = (warp + NW * t) * RL;                  // first row of the stage, from v0
+            const uint32_t n = (uint32_t)min(RL, nrows - r) * (uint32_t)p.row_bytes;
+            mbar_arrive_expect_tx(wbar + 8 * slot, n);
+            bulk_g2s(slot0 + slot * stage_bytes, wrow0 + (int64_t)r * p.row_bytes, n, wbar + 8 * slot);
+            return;
+        }
         const int bl = t / npc, pc = t - (t / npc) * npc;
         const int ca = cbeg + pc * PCS;
         int64_t poff, pbytes;
