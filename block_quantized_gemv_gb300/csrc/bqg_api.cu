@@ -270,7 +270,7 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     if (M > 2) return BQG_ERR_UNSUPPORTED_SHAPE;
     static const bool off = env_int("BQG_NO_LPR", 0) != 0;
     if (off) return BQG_ERR_UNSUPPORTED_SHAPE;
-    static const int big_kb = std::max(16, std::min(220, env_int("BQG_LPR_KB", 110)));
+    static const int big_kb = std::max(16, std::min(220, env_int("BQG_LPR_KB", 113)));
     static const int small_kb = std::max(16, std::min(110, env_int("BQG_LPR_OVERLAP_KB", 54)));
     static const int share_kb = env_int("BQG_OVERLAP_SHARE_KB", 0);       // measured: off
     static const int force_L = env_int("BQG_LPR_L", 0);
@@ -332,7 +332,10 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     const int slots = (int)std::min<int64_t>(64, budget / stage);
     int ng = std::max(1, std::min(max_warps, slots / 2));
     int D = std::max(1, slots / ng);
-    if (force_D > 0) { D = force_D; ng = std::max(1, std::min(max_warps, slots / D)); }
+    // measured on the decode shapes: q8_1 activations (short, cheap rows)
+    // gain more from twelve warps with one slot each than from double slots
+    const int want_D = (force_D > 0) ? force_D : (xf == X_Q8_1) ? 1 : 0;
+    if (want_D > 0) { D = want_D; ng = std::max(1, std::min(max_warps, slots / D)); }
     g.ng = ng;
     g.NS = D;
     g.TPR = 32 * g.ng;
