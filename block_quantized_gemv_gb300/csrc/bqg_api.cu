@@ -24,10 +24,10 @@ cudaError_t gemv_lpr_run_bf16(const GemvParams &, int, dim3, int, size_t, cudaSt
 cudaError_t gemv_lpr_run_q8_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_lpr_run_q4_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
-int gemv_x_stage_bytes_bf16(int, int);
-int gemv_x_stage_bytes_q8_0(int, int);
-int gemv_x_stage_bytes_q4_0(int, int);
-int gemv_x_stage_bytes_q4_0_q8_1(int, int);
+int gemv_x_stage_bytes_bf16(int, int, int);
+int gemv_x_stage_bytes_q8_0(int, int, int);
+int gemv_x_stage_bytes_q4_0(int, int, int);
+int gemv_x_stage_bytes_q4_0_q8_1(int, int, int);
 cudaError_t launch_quantize_q8_1(const void *, int, void *, int, int64_t, cudaStream_t, bool);
 cudaError_t launch_rmsnorm_q8_1(const void *, int, const float *, float, void *, int, int64_t, cudaStream_t, bool);
 cudaError_t launch_quantize_weights(int, const float *, void *, int64_t, int64_t, cudaStream_t);
@@ -124,16 +124,17 @@ LprFn lpr_runner(int wf, int xf)
     if (wf == W_Q8_0) return gemv_lpr_run_q8_0;
     return gemv_lpr_run_q4_0;
 }
-int x_stage_bytes(int wf, int xf, int nc, int nb)
+// staged bytes of one activation row (bf16 rows staged as bf16 when bf16 != 0, else fp32)
+int x_stage_bytes(int wf, int xf, int nc, int nb, int bf16)
 {
-    if (xf == X_Q8_1) return gemv_x_stage_bytes_q4_0_q8_1(nc, nb);
-    if (wf == W_BF16) return gemv_x_stage_bytes_bf16(nc, nb);
-    if (wf == W_Q8_0) return gemv_x_stage_bytes_q8_0(nc, nb);
-    return gemv_x_stage_bytes_q4_0(nc, nb);
+    if (xf == X_Q8_1) return gemv_x_stage_bytes_q4_0_q8_1(nc, nb, 0);
+    if (wf == W_BF16) return gemv_x_stage_bytes_bf16(nc, nb, bf16);
+    if (wf == W_Q8_0) return gemv_x_stage_bytes_q8_0(nc, nb, bf16);
+    return gemv_x_stage_bytes_q4_0(nc, nb, bf16);
 }
 
 struct GemvPlan {
-    bool lpr;               // lanes-per-row kernel (M <= 2)
+    bool lpr;               // lanes-per-row kernel
     int L, x_off, x_row_bytes, xraw_off, early, rl, piece_chunks, wg, ng;
     int C, TPR, RG, RPS, nc, cps, splits, threads, ncons, S, NS, stride, win_stages, part_off, bar_off, ctas;
     dim3 grid;
@@ -153,7 +154,7 @@ constexpr int kStageBudget = 100 * 1024;
 //   BQG_LPR_KB, BQG_LPR_OVERLAP_KB, BQG_OVERLAP_SHARE_KB, BQG_LPR_L, BQG_LPR_D,
 //   BQG_LPR_EARLY, BQG_LPR_RL, BQG_LPR_PIECE, BQG_LPR_STAGE_KB
 //                    lanes-per-row geometry (see plan_lpr)
-//   BQG_NO_LPR       1: serve M <= 2 with the K-slice kernel
+//   BQG_NO_LPR       1: serve every M with the K-slice kernel
 int env_int(const char *name, int dflt)
 {
     const char *v = getenv(name);
@@ -254,7 +255,7 @@ int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevI
 }
 
 
-// Launch geometry of the lanes-per-row kernel (M <= 2).  Returns
+// Launch geometry of the lanes-per-row kernel (M = 1, 2, 4, 8).  Returns
 // BQG_ERR_UNSUPPORTED_SHAPE when the staged activations would not fit, in
 // which case the K-slice kernel (plan_gemv) serves the call.
 //
@@ -267,7 +268,7 @@ int plan_gemv(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevI
 int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevInfo &dev, int device,
              GemvPlan *pl)
 {
-    if (M > 2) return BQG_ERR_UNSUPPORTED_SHAPE;
+    if (M != 1 && M != 2 && M != 4 && M != 8) return BQG_ERR_UNSUPPORTED_SHAPE;
     static const bool off = env_int("BQG_NO_LPR", 0) != 0;
     if (off) return BQG_ERR_UNSUPPORTED_SHAPE;
     static const int big_kb = std::max(16, std::min(220, env_int("BQG_LPR_KB", 113)));
@@ -288,12 +289,14 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     g.splits = 1;
     if (Nv < (int64_t)dev.sms * 4)
         g.splits = (int)std::min<int64_t>(maxs, ((int64_t)dev.sms * 4 + Nv - 1) / std::max<int64_t>(Nv, 1));
-    g.x_row_bytes = (x_stage_bytes(wf, xf, g.nc, nb) + 15) / 16 * 16;
-    // staged activations plus their raw copy (the 16-byte-aligned span
-    // around X: up to 15 bytes of slack on either side)
-    const int xraw = (int)((M * ((xf == X_Q8_1) ? (int64_t)nb * Q8_1_BYTES : K * 2) + 30) / 16 * 16);
+    // M = 4, 8 with bf16 activations: rows staged as bf16, copied in place
+    // (no raw copy); else staged rows plus their raw copy (the
+    // 16-byte-aligned span around X: up to 15 bytes of slack on either side)
+    const bool bf16s = (M >= 4 && xf == X_BF16);
+    g.x_row_bytes = (x_stage_bytes(wf, xf, g.nc, nb, bf16s ? 1 : 0) + 15) / 16 * 16;
+    const int xraw = bf16s ? 0 : (int)((M * ((xf == X_Q8_1) ? (int64_t)nb * Q8_1_BYTES : K * 2) + 30) / 16 * 16);
     const int xbytes = M * g.x_row_bytes + xraw + 16;
-    if (xbytes > 64 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
+    if (xbytes > 80 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
     g.cps = g.nc;
     if (g.splits > 1) {
         g.cps = ((g.nc + g.splits - 1) / g.splits + align - 1) / align * align;
@@ -311,6 +314,7 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     // rows are short, so the copy stays large), one row for the others
     int rl = (M == 1 && xf == X_Q8_1) ? 2 : 1;
     if (force_rl == 1 || force_rl == 2 || (force_rl == 4 && M == 1)) rl = force_rl;
+    if (force_rl == 0 && M >= 4) rl = 1;
     if (unit == 2 && (rl & 1)) rl = 2;
     g.rl = rl;
     g.wg = 1;
@@ -334,7 +338,7 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     int D = std::max(1, slots / ng);
     // measured on the decode shapes: q8_1 activations (short, cheap rows)
     // gain more from twelve warps with one slot each than from double slots
-    const int want_D = (force_D > 0) ? force_D : (xf == X_Q8_1) ? 1 : 0;
+    const int want_D = (force_D > 0) ? force_D : (xf == X_Q8_1 || M >= 4) ? 1 : 0;
     if (want_D > 0) { D = want_D; ng = std::max(1, std::min(max_warps, slots / D)); }
     g.ng = ng;
     g.NS = D;

@@ -663,9 +663,13 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
 // Staged activations for the lanes-per-row kernel.  Chunk c of activation
 // row m is P pieces of 16 bytes; piece p of chunks 32u .. 32u+31 is one run
 // of 512 bytes, so lanes reading consecutive chunks hit distinct banks.
-// q8_1 rows add, per block, (d as float, exact sum of codes) after the runs.
+// Pieces hold four fp32 (M <= 2) or eight bf16 (X_BF16: M = 4, 8, where
+// fp32 rows would not fit beside the weight stages).  q8_1 rows add, per
+// block, (d as float, exact sum of codes) after the runs.
 // ---------------------------------------------------------------------------
-template <int WF, int XF> struct XPieces { static constexpr int P = ChunkTraits<WF>::E / 4; };   // fp32
+template <int WF, int XF> struct XPieces {
+    static constexpr int P = ChunkTraits<WF>::E / ((XF == X_BF16) ? 8 : 4);
+};
 template <> struct XPieces<W_Q4_0, X_Q8_1> { static constexpr int P = 2; };                    // 32 codes
 
 template <int WF, int XF>
@@ -717,6 +721,30 @@ __device__ __forceinline__ void expand_x(const GemvParams &p, const uint8_t *raw
     }
 }
 
+// bf16 activation rows copied as they are (row m at m * x_row_bytes) into
+// the staged bf16 layout, in place: for 32-element blocks (q8_0, q4_0
+// weights) piece j (elements 8j .. 8j+7) of block s of tile t moves from
+// t * 2048 + s * 64 + j * 16 to t * 2048 + j * 512 + s * 16.  A tile's
+// 2 KiB map onto themselves, so each warp permutes whole tiles alone.  For
+// bf16 weights (one piece per chunk) the copied rows are already staged.
+template <int WF>
+__device__ __forceinline__ void permute_x_bf16(const GemvParams &p, uint8_t *xs, int M, int warp, int nwarps, int lane)
+{
+    if constexpr (WF != W_BF16) {
+        const int T = (p.nb + 31) / 32;
+        for (int r = warp; r < M * T; r += nwarps) {
+            uint8_t *base = xs + (size_t)(r / T) * p.x_row_bytes + (size_t)(r - (r / T) * T) * 2048;
+            uint4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) v[k] = *reinterpret_cast<const uint4 *>(base + lane * 64 + k * 16);
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; k++) *reinterpret_cast<uint4 *>(base + k * 512 + lane * 16) = v[k];
+            __syncwarp();
+        }
+    }
+}
+
 template <int WF, int XF>
 __device__ __forceinline__ void lds_x(XSlice<WF, XF> &x, const uint8_t *xr, int c, int runs)
 {
@@ -753,7 +781,9 @@ template <> struct TileTraits<W_BF16> { static constexpr int CPT = 32, TW = 512;
 template <> struct TileTraits<W_Q8_0> { static constexpr int CPT = 64, TW = Q8_0_TILE; };
 template <> struct TileTraits<W_Q4_0> { static constexpr int CPT = 32, TW = Q4_0_TILE; };
 // staged activation bytes of one tile
-template <int WF, int XF> struct TileX { static constexpr int TX = (WF == W_BF16) ? 1024 : 4096; };
+template <int WF, int XF> struct TileX {
+    static constexpr int TX = ((WF == W_BF16) ? 1024 : 4096) / ((XF == X_BF16) ? 2 : 1);
+};
 template <> struct TileX<W_Q4_0, X_Q8_1> { static constexpr int TX = 1024; };
 
 // sum over the 16 int8 codes of c of q * x (x: 16 fp32 in four float4), into
@@ -841,7 +871,24 @@ __device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t 
     auto body = [&](int t) {
         const uint8_t *wt = w0 + t * TW;
         const uint8_t *xt = x0 + t * TX;
-        if constexpr (WF == W_BF16) {
+        if constexpr (WF == W_BF16 && XF == X_BF16) {
+            // weights converted once, each activation piece (8 bf16) once per row m
+            float w[RL][8];
+#pragma unroll
+            for (int i = 0; i < RL; i++) {
+                const uint4 c = *reinterpret_cast<const uint4 *>(wt + i * row_stride);
+                bf16x8_to_f32(c, w[i]);
+            }
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                float x[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xt + m * x_row_bytes), x);
+#pragma unroll
+                for (int i = 0; i < RL; i++)
+#pragma unroll
+                    for (int k = 0; k < 8; k += 2) ffma2(acc[i][m][0], acc[i][m][1], w[i][k], w[i][k + 1], x[k], x[k + 1]);
+            }
+        } else if constexpr (WF == W_BF16) {
             uint4 c[RL];
 #pragma unroll
             for (int i = 0; i < RL; i++) c[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride);
@@ -858,6 +905,52 @@ __device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t 
                     ffma2(s0, s1, bf16_lo(c[i].w), bf16_hi(c[i].w), xb.z, xb.w);
                 }
             }
+        } else if constexpr (WF == W_Q8_0 && XF == X_BF16) {
+            // unit = block sub; codes dequantized once per 8-element piece,
+            // each activation piece loaded once per row m
+            constexpr float OFF = 8388608.0f + 128.0f;
+            uint4 c0[RL], c1[RL];
+            float d[RL];
+#pragma unroll
+            for (int i = 0; i < RL; i++) {
+                c0[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride);
+                c1[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride + 512);
+                d[i] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(wt + i * row_stride + 1024 - 14 * sub));
+            }
+            float sm[RL][M][2];
+#pragma unroll
+            for (int i = 0; i < RL; i++)
+#pragma unroll
+                for (int m = 0; m < M; m++) sm[i][m][0] = sm[i][m][1] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                float e[RL][8];
+#pragma unroll
+                for (int i = 0; i < RL; i++) {
+                    const uint32_t wa = (j == 0) ? c0[i].x : (j == 1) ? c0[i].z : (j == 2) ? c1[i].x : c1[i].z;
+                    const uint32_t wb = (j == 0) ? c0[i].y : (j == 1) ? c0[i].w : (j == 2) ? c1[i].y : c1[i].w;
+                    const uint32_t ua = wa ^ 0x80808080u, ub = wb ^ 0x80808080u;
+                    e[i][0] = byte_plus_2p23<0>(ua); e[i][1] = byte_plus_2p23<1>(ua);
+                    e[i][2] = byte_plus_2p23<2>(ua); e[i][3] = byte_plus_2p23<3>(ua);
+                    e[i][4] = byte_plus_2p23<0>(ub); e[i][5] = byte_plus_2p23<1>(ub);
+                    e[i][6] = byte_plus_2p23<2>(ub); e[i][7] = byte_plus_2p23<3>(ub);
+#pragma unroll
+                    for (int k = 0; k < 8; k += 2) fadd2(e[i][k], e[i][k + 1], -OFF);
+                }
+#pragma unroll
+                for (int m = 0; m < M; m++) {
+                    float x[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xt + m * x_row_bytes + j * 512), x);
+#pragma unroll
+                    for (int i = 0; i < RL; i++)
+#pragma unroll
+                        for (int k = 0; k < 8; k += 2) ffma2(sm[i][m][0], sm[i][m][1], e[i][k], e[i][k + 1], x[k], x[k + 1]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RL; i++)
+#pragma unroll
+                for (int m = 0; m < M; m++) acc[i][m][0] = fmaf(sm[i][m][0] + sm[i][m][1], d[i], acc[i][m][0]);
         } else if constexpr (WF == W_Q8_0) {
             // unit = block sub: codes 0..15 at +0, 16..31 at +512, scale at 1024 + 2 sub
             uint4 c0[RL], c1[RL];
@@ -901,6 +994,53 @@ __device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t 
                     acc[i][m][0] = fmaf(d[i] * ds.x, (float)q4q8_sumi(c[i], xl, xh, __float_as_int(ds.y)),
                                         acc[i][m][0]);
             }
+        } else if constexpr (XF == X_BF16) {
+            // q4_0 against bf16 activations: unit = block sub; piece j
+            // (elements 8j .. 8j+7) is the low (j < 2) or high nibbles of
+            // words 2(j&1), 2(j&1)+1
+            constexpr float OFF = 8388608.0f + 8.0f;
+            uint4 c[RL];
+            float d[RL];
+#pragma unroll
+            for (int i = 0; i < RL; i++) {
+                c[i] = *reinterpret_cast<const uint4 *>(wt + i * row_stride);
+                d[i] = half_bits_to_float(*reinterpret_cast<const uint16_t *>(wt + i * row_stride + 512 - 14 * sub));
+            }
+            float sm[RL][M][2];
+#pragma unroll
+            for (int i = 0; i < RL; i++)
+#pragma unroll
+                for (int m = 0; m < M; m++) sm[i][m][0] = sm[i][m][1] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                float e[RL][8];
+#pragma unroll
+                for (int i = 0; i < RL; i++) {
+                    const uint32_t w0 = (j & 1) ? c[i].z : c[i].x;
+                    const uint32_t w1 = (j & 1) ? c[i].w : c[i].y;
+                    const uint32_t ua = ((j < 2) ? w0 : (w0 >> 4)) & 0x0f0f0f0fu;
+                    const uint32_t ub = ((j < 2) ? w1 : (w1 >> 4)) & 0x0f0f0f0fu;
+                    e[i][0] = byte_plus_2p23<0>(ua); e[i][1] = byte_plus_2p23<1>(ua);
+                    e[i][2] = byte_plus_2p23<2>(ua); e[i][3] = byte_plus_2p23<3>(ua);
+                    e[i][4] = byte_plus_2p23<0>(ub); e[i][5] = byte_plus_2p23<1>(ub);
+                    e[i][6] = byte_plus_2p23<2>(ub); e[i][7] = byte_plus_2p23<3>(ub);
+#pragma unroll
+                    for (int k = 0; k < 8; k += 2) fadd2(e[i][k], e[i][k + 1], -OFF);
+                }
+#pragma unroll
+                for (int m = 0; m < M; m++) {
+                    float x[8];
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xt + m * x_row_bytes + j * 512), x);
+#pragma unroll
+                    for (int i = 0; i < RL; i++)
+#pragma unroll
+                        for (int k = 0; k < 8; k += 2) ffma2(sm[i][m][0], sm[i][m][1], e[i][k], e[i][k + 1], x[k], x[k + 1]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RL; i++)
+#pragma unroll
+                for (int m = 0; m < M; m++) acc[i][m][0] = fmaf(sm[i][m][0] + sm[i][m][1], d[i], acc[i][m][0]);
         } else {
             // q4_0 against fp32 activations: unit = block sub
             uint4 c[RL];
@@ -927,7 +1067,7 @@ __device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t 
 }
 
 // ---------------------------------------------------------------------------
-// Lanes-per-row kernel (M = 1, 2).  There is no producer warp: each of the
+// Lanes-per-row kernel (M = 1, 2, 4, 8).  There is no producer warp: each of the
 // CTA's NW warps streams its own work.  The CTA's rows are cut into blocks
 // of RL consecutive rows (a gate/up block holds RL/2 gate rows, then the
 // matching up rows), and block b belongs to warp b % NW.  A block is
@@ -1022,10 +1162,20 @@ __global__ void __launch_bounds__(384, 2) gemv_lpr_kernel(const GemvParams p)
     // never crosses a page), as bulk copies need 16-byte alignment.
     const uintptr_t xa = reinterpret_cast<uintptr_t>(p.X);
     const int xoff = (int)(xa & 15);
-    const uint32_t xcopy = (uint32_t)((xoff + M * x_src_row_bytes<XF>(p) + 15) & ~15ll);
-    if (tid == 0) {
-        mbar_arrive_expect_tx(xbar, xcopy);
-        bulk_g2s(smem_u32(smem + p.xraw_off), reinterpret_cast<const void *>(xa - xoff), xcopy, xbar);
+    if constexpr (XF == X_BF16) {
+        // bf16 rows (16-byte aligned) straight into their staged rows
+        if (tid == 0) {
+            const uint32_t rb = (uint32_t)p.K * 2;
+            mbar_arrive_expect_tx(xbar, (uint32_t)M * rb);
+            for (int m = 0; m < M; m++)
+                bulk_g2s(smem_u32(xs + (size_t)m * p.x_row_bytes), p.X + (size_t)m * rb, rb, xbar);
+        }
+    } else {
+        const uint32_t xcopy = (uint32_t)((xoff + M * x_src_row_bytes<XF>(p) + 15) & ~15ll);
+        if (tid == 0) {
+            mbar_arrive_expect_tx(xbar, xcopy);
+            bulk_g2s(smem_u32(smem + p.xraw_off), reinterpret_cast<const void *>(xa - xoff), xcopy, xbar);
+        }
     }
     __syncthreads();
     if (lane == 0)
@@ -1035,7 +1185,10 @@ __global__ void __launch_bounds__(384, 2) gemv_lpr_kernel(const GemvParams p)
         atomicExch(&g_gemv_error, 1);
         s_abort = 1;
     }
-    expand_x<WF, XF>(p, smem + p.xraw_off + xoff, xs, M, tid, blockDim.x);
+    if constexpr (XF == X_BF16)
+        permute_x_bf16<WF>(p, xs, M, warp, NW, lane);
+    else
+        expand_x<WF, XF>(p, smem + p.xraw_off + xoff, xs, M, tid, blockDim.x);
     __syncthreads();
 
     const int ds_off = ((p.nc + 31) / 32) * XPieces<WF, XF>::P * 512;   // q8_1 (d, sum) table
@@ -1170,13 +1323,18 @@ template <int WF, int XF>
 __host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, int threads, size_t smem,
                                        cudaStream_t stream, bool pdl, int *occupancy)
 {
-    constexpr int XR = (XF == X_BF16) ? X_F32 : XF;      // staged bf16 activations are fp32
+    constexpr int XR = (XF == X_BF16) ? X_F32 : XF;      // M <= 2: bf16 activations staged as fp32
     const int rl = p.rl;
     if (M == 1 && rl == 1) return gemv_lpr_launch_one<WF, XR, 1, 1>(p, grid, threads, smem, stream, pdl, occupancy);
     if (M == 1 && rl == 2) return gemv_lpr_launch_one<WF, XR, 1, 2>(p, grid, threads, smem, stream, pdl, occupancy);
     if (M == 1 && rl == 4) return gemv_lpr_launch_one<WF, XR, 1, 4>(p, grid, threads, smem, stream, pdl, occupancy);
     if (M == 2 && rl == 1) return gemv_lpr_launch_one<WF, XR, 2, 1>(p, grid, threads, smem, stream, pdl, occupancy);
     if (M == 2 && rl == 2) return gemv_lpr_launch_one<WF, XR, 2, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+    // M = 4, 8: bf16 activations staged as bf16
+    if (M == 4 && rl == 1) return gemv_lpr_launch_one<WF, XF, 4, 1>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 4 && rl == 2) return gemv_lpr_launch_one<WF, XF, 4, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 8 && rl == 1) return gemv_lpr_launch_one<WF, XF, 8, 1>(p, grid, threads, smem, stream, pdl, occupancy);
+    if (M == 8 && rl == 2) return gemv_lpr_launch_one<WF, XF, 8, 2>(p, grid, threads, smem, stream, pdl, occupancy);
     return cudaErrorInvalidValue;
 }
 

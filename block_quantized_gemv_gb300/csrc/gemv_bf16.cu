@@ -13,5 +13,5 @@ cudaError_t gemv_lpr_run_bf16(const GemvParams &p, int M, dim3 grid, int threads
 {
     return gemv_lpr_dispatch<W_BF16, X_BF16>(p, M, grid, threads, smem, stream, pdl, occupancy);
 }
-int gemv_x_stage_bytes_bf16(int nc, int nb) { return x_stage_row_bytes<W_BF16, X_F32>(nc, nb); }
+int gemv_x_stage_bytes_bf16(int nc, int nb, int bf16) { return bf16 ? x_stage_row_bytes<W_BF16, X_BF16>(nc, nb) : x_stage_row_bytes<W_BF16, X_F32>(nc, nb); }
 }  // namespace bqg
