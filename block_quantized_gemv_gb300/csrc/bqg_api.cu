@@ -314,7 +314,9 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     // rows are short, so the copy stays large), one row for the others
     int rl = (M == 1 && xf == X_Q8_1) ? 2 : 1;
     if (force_rl == 1 || force_rl == 2 || (force_rl == 4 && M == 1)) rl = force_rl;
-    if (force_rl == 0 && M >= 4) rl = 1;
+    // M = 4, 8 (measured on the sweep shapes): two rows per lane, but one
+    // for q8_0 at M = 8, whose dequant registers then spill
+    if (force_rl == 0 && M >= 4) rl = (wf == W_Q8_0 && M == 8) ? 1 : 2;
     if (unit == 2 && (rl & 1)) rl = 2;
     g.rl = rl;
     g.wg = 1;
@@ -332,7 +334,7 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     g.stride = (int)range_bytes(wf, std::min(g.piece_chunks, g.cps));
     const int64_t stage = (int64_t)g.S * g.stride;
     if (budget < stage) return BQG_ERR_UNSUPPORTED_SHAPE;
-    const int max_warps = overlap ? 8 : kLprMaxWarps;
+    const int max_warps = (overlap || M >= 4) ? 8 : kLprMaxWarps;   // M >= 4: the kernel's 256-thread bound
     const int slots = (int)std::min<int64_t>(64, budget / stage);
     int ng = std::max(1, std::min(max_warps, slots / 2));
     int D = std::max(1, slots / ng);

@@ -1085,8 +1085,12 @@ __device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t 
 // block; after its last piece one warp shuffle reduction per output
 // finishes the block, which lane 0 stores.
 // ---------------------------------------------------------------------------
+// M = 4, 8: at most eight warps, so that two rows per lane (half the
+// shared-memory activation reads per weight) fit in registers
+template <int M> struct LprThreads { static constexpr int value = (M >= 4) ? 256 : 384; };
+
 template <int WF, int XF, int M, int RL>
-__global__ void __launch_bounds__(384, 2) gemv_lpr_kernel(const GemvParams p)
+__global__ void __launch_bounds__(LprThreads<M>::value, 2) gemv_lpr_kernel(const GemvParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
