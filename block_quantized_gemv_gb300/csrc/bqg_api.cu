@@ -312,7 +312,9 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     g.L = 32;
     // measured on the decode shapes: two rows per warp for q4_0 x q8_1 (its
     // rows are short, so the copy stays large), one row for the others
-    int rl = (M == 1 && xf == X_Q8_1) ? 2 : 1;
+    // measured on the decode and sweep shapes: two rows per lane for q8_1
+    // activations (M = 1, 2) and for q4_0 x bf16 at M = 1, one otherwise
+    int rl = ((M <= 2 && xf == X_Q8_1) || (M == 1 && wf == W_Q4_0)) ? 2 : 1;
     if (force_rl == 1 || force_rl == 2 || (force_rl == 4 && M == 1)) rl = force_rl;
     // M = 4, 8 (measured on the sweep shapes): two rows per lane, but one
     // for q8_0 at M = 8, whose dequant registers then spill
@@ -338,9 +340,11 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     const int slots = (int)std::min<int64_t>(64, budget / stage);
     int ng = std::max(1, std::min(max_warps, slots / 2));
     int D = std::max(1, slots / ng);
-    // measured on the decode shapes: q8_1 activations (short, cheap rows)
-    // gain more from twelve warps with one slot each than from double slots
-    const int want_D = (force_D > 0) ? force_D : (xf == X_Q8_1 || M >= 4) ? 1 : 0;
+    // measured: q8_1 activations, q4_0 weights and M >= 2 gain more from
+    // more warps with one slot each than from double slots; bf16 and q8_0
+    // weights at M = 1 keep two
+    const bool one_slot = xf == X_Q8_1 || M >= 2 || wf == W_Q4_0;
+    const int want_D = (force_D > 0) ? force_D : one_slot ? 1 : 0;
     if (want_D > 0) { D = want_D; ng = std::max(1, std::min(max_warps, slots / D)); }
     g.ng = ng;
     g.NS = D;
