@@ -3,23 +3,24 @@
 // The tiled prefill GEMM of "llama-3x-prompt-speed" ("the tile"): a weight
 // tile is unpacked once and serves every activation row of the tile,
 // instead of being unpacked once per row.  Here the unit of work is 128
-// weight rows x 128 activation rows; per k-step of 64:
-//   * warp 14, lane 0 stages the raw weight codes and scales of four k-steps
-//     at a time into shared memory with two-dimensional TMA copies (128 rows
+// weight rows x 128 activation rows; per stage of 128 along K:
+//   * warp 14, lane 0 stages the raw weight codes and scales of two stages
+//     at a time (eight q4_0 blocks per row) into shared memory with two-dimensional TMA copies (128 rows
 //     x 128 bytes of codes in the 128-byte swizzle, 128 rows x 16 bytes of
 //     scales), so the weight stream is coalesced;
 //   * warps 1-8 (one weight block of one weight row per thread) read their
 //     block's codes and scale from there (conflict-free thanks to the
 //     swizzle), dequantize q * d or (q - 8) * d exactly in fp32, round once to
-//     bf16 and store the 128 x 64 bf16 tile straight into tensor memory
+//     bf16 and store the 128 x 128 bf16 tile straight into tensor memory
 //     (tcgen05.st: lane = weight row, two k per column), where the MMA reads
 //     its A operand.  Shared memory then carries only the
 //     activation tiles: with A staged there too, its bandwidth (dequant
 //     writes, TMA writes and both MMA operands, 64 KiB per k-step) bounded
 //     the loop at twice the MMA time;
-//   * warp 13, lane 0 loads the matching 128 x 64 bf16 activation tile with
-//     one TMA copy (same swizzle) as soon as the stage is free;
-//   * warp 0, lane 0 issues four tcgen05.mma.kind::f16 (A from tensor
+//   * warp 13, lane 0 loads the matching 128 x 128 bf16 activation tile with
+//     two TMA copies of one 64-wide swizzle atom each as soon as the stage
+//     is free (a trailing half stage when K % 128 == 64);
+//   * warp 0, lane 0 issues eight tcgen05.mma.kind::f16 (A from tensor
 //     memory, B from shared memory; M = 128 weight rows, N = 128
 //     activations, K = 16) accumulating fp32 in tensor memory as soon as both
 //     halves of the stage are in place; tcgen05.commit frees the stage.  It
@@ -29,7 +30,7 @@
 //     tcgen05.ld (each warp its 32 lanes = 32 weight rows) and store
 //     Y[m][n] coalesced along n.
 // Tensor memory (512 columns): two 128-column accumulators, so the epilogue
-// of one unit overlaps the MMAs of the next, then the NSTAGE A slots of 32
+// of one unit overlaps the MMAs of the next, then the NSTAGE A slots of 64
 // columns.  The kernel is persistent (one
 // CTA per SM).  Every mbarrier wait is bounded: on a timeout the kernel sets
 // g_gemm_error, stops issuing work, drains what it started and frees TMEM.

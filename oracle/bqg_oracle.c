@@ -187,8 +187,10 @@ int ref_quantize(int fmt, const float *x, int64_t rows, int64_t K, uint8_t *out)
  * ([MI50] hypothesis ledger: fusing neighbouring steps and epilogues;
  * [RX6700] Approach & Methodology: the Q8_1 activation of the matvec).
  * Reading (the pages name the fusion, not its arithmetic), per row:
- *     s   = sum_k x_k^2               in fp64, k in order (exact for bf16
- *                                     inputs: each square has 16 bits)
+ *     s   = sum_k x_k^2               in fp64, k in order (each square of a
+ *                                     bf16 input is exact; the sum is exact
+ *                                     while the squares span less than 2^37,
+ *                                     as for N(0,1) rows, else fp64-rounded)
  *     r   = fp32( 1 / sqrt(s / K + eps) )    (fp64 sqrt and division)
  *     y_k = fp32( fp32(x_k * r) * gamma_k )  (gamma NULL: y_k = fp32(x_k * r))
  * and y is encoded into q8_1 blocks by encode_q8_1 above.
