@@ -273,19 +273,23 @@ class DecodeLayerArm(Arm):
     """q4_0 x q8_1 decode layer: quantize(x), QKV, gate+up+SwiGLU, quantize(h), down.
     With fused_norm the layer starts from the raw activation row: its first
     step is the fused RMSNorm -> q8_1 encoder, and the gate+up epilogue writes
-    h as q8_1 for the down projection (four launches instead of five)."""
+    h as q8_1 for the down projection (four launches instead of five).  With
+    persistent the whole layer (q8_1 of x, QKV, gate+up+SwiGLU->q8_1, down) is
+    one cooperative launch with a grid barrier before the down projection."""
 
-    def __init__(self, seed=5, K=4096, Nq=4096, Nff=11008, fused_norm=False):
+    def __init__(self, seed=5, K=4096, Nq=4096, Nff=11008, fused_norm=False, persistent=False):
         import torch
         import block_quantized_gemv_gb300 as bqg
         from block_quantized_gemv_gb300 import synth
         super().__init__()
         self.bqg, self.torch = bqg, torch
-        self.fused_norm = fused_norm
+        self.fused_norm, self.persistent = fused_norm, persistent
         self.name = (f"q4_0 x q8_1 decode layer M=1 (QKV 3x{Nq}x{K}, gate+up 2x{Nff}x{K}, down {K}x{Nff})"
-                     + (", fused RMSNorm->q8_1 and SwiGLU->q8_1" if fused_norm else ""))
-        self.kernel_key = "decode_layer_q4_0_q8_1" + ("_fused_norm" if fused_norm else "")
-        self.launches_per_call = 4 if fused_norm else 5
+                     + (", fused RMSNorm->q8_1 and SwiGLU->q8_1" if fused_norm else "")
+                     + (", one persistent launch" if persistent else ""))
+        self.kernel_key = ("decode_layer_q4_0_q8_1" + ("_fused_norm" if fused_norm else "")
+                           + ("_persistent" if persistent else ""))
+        self.launches_per_call = 1 if persistent else 4 if fused_norm else 5
         self.K, self.Nq, self.Nff = K, Nq, Nff
 
         def mk(N, KK, sd):
@@ -310,13 +314,19 @@ class DecodeLayerArm(Arm):
                       "ws_qkv": bqg.workspace(bqg.OP_QKV_Q4_0_Q8_1, 1, 3 * Nq, K),
                       "ws_gu": bqg.workspace(bqg.OP_GATE_UP_Q8_1_Q4_0_Q8_1 if fused_norm else
                                              bqg.OP_GATE_UP_Q4_0_Q8_1, 1, Nff, K),
-                      "ws_d": bqg.workspace(bqg.OP_GEMV_Q4_0_Q8_1, 1, K, Nff)})
+                      "ws_d": bqg.workspace(bqg.OP_GEMV_Q4_0_Q8_1, 1, K, Nff),
+                      "ws_layer": bqg.workspace(bqg.OP_DECODE_LAYER_Q4_0_Q8_1, 1, Nff, K) if persistent else None})
             self.sets.append(s)
         self.x_host = x.cpu().pin_memory()
         self.y_host = torch.empty((1, K), dtype=torch.float32).pin_memory()
 
     def call(self, i):
         b, s = self.bqg, self.sets[i % self.R]
+        if self.persistent:
+            b.decode_layer_q4_0_q8_1(s["x"], s["x"], s["Wq"], s["Wk"], s["Wv"], s["Wg"], s["Wu"], s["Wd"], self.Nq,
+                                     self.Nq, self.Nff, self.K, out=(s["q"], s["k"], s["v"], s["y"]),
+                                     ws=s["ws_layer"])
+            return
         if self.fused_norm:
             b.rmsnorm_quantize_q8_1(s["x"], None, 1e-5, out=s["xq"])
         else:
@@ -577,6 +587,7 @@ def main():
              GemmArm()]
     if args.suite == "full":
         other += [GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096), DecodeLayerArm(), DecodeLayerArm(fused_norm=True),
+                  DecodeLayerArm(persistent=True),
                   GemmArm(fmt=bqg.Q8_0)]
         for M in (1, 2, 4, 8):
             for f in (bqg.BF16, bqg.Q8_0, bqg.Q4_0):

@@ -18,7 +18,7 @@ import torch
 BF16, Q8_0, Q4_0, Q8_1, F32 = 0, 1, 2, 3, 4
 OP_GEMV_BF16, OP_GEMV_Q8_0, OP_GEMV_Q4_0, OP_GEMV_Q4_0_Q8_1 = 0, 1, 2, 3
 OP_QKV_Q4_0_Q8_1, OP_GATE_UP_Q4_0_Q8_1, OP_GEMM_Q4_0_BF16 = 4, 5, 6
-OP_GATE_UP_Q8_1_Q4_0_Q8_1, OP_GEMM_Q8_0_BF16 = 7, 8
+OP_GATE_UP_Q8_1_Q4_0_Q8_1, OP_GEMM_Q8_0_BF16, OP_DECODE_LAYER_Q4_0_Q8_1 = 7, 8, 9
 BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q8_1: 36}
 QK = 32
 
@@ -39,6 +39,8 @@ EXPORTS = {
     "bqg_gemv_q4_0_q8_1_qkv": (["p", "p", "p", "p", "p", "p", "p", "i", "i64", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemv_q4_0_q8_1_gate_up_swiglu": (["p", "p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1": (["p", "p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
+    "bqg_decode_layer_q4_0_q8_1": (["p", "p", "i", "p", "p", "p", "p", "p", "p", "p", "p", "p", "p", "i", "i64",
+                                    "i64", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemm_q4_0_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemm_q8_0_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_debug_q4_0_q8_1_block_dots": (["p", "p", "p", "i64", "i64", "p"], "i"),
@@ -264,6 +266,38 @@ def gemv_q4_0_q8_1_gate_up_swiglu_q8_1(Wg, Wu, Xq, N, K, out=None, ws=None, stre
                                                          wsp, wsb, _stream(stream)),
            "bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1")
     return out
+
+
+def decode_layer_q4_0_q8_1(xa, xb, Wq, Wk, Wv, Wg, Wu, Wd, Nq, Nkv, Nff, K, out=None, ws=None, stream=None):
+    """One decode layer (M = 1) in one persistent launch: q8_1 of xa and xb,
+    QKV from xa, gate+up+SwiGLU (h as q8_1) from xb, down projection of h.
+    xa, xb: (1, K) bf16 or fp32.  Returns (Yq, Yk, Yv, Y).  `ws`
+    (workspace(OP_DECODE_LAYER_Q4_0_Q8_1, 1, Nff, K)) must start zero-filled;
+    it also holds h's q8_1 blocks (see `layer_hq`)."""
+    if xa.dtype not in (torch.bfloat16, torch.float32) or xb.dtype != xa.dtype:
+        raise TypeError("xa and xb must both be bfloat16 or both float32")
+    dt = F32 if xa.dtype == torch.float32 else BF16
+    nx = K * xa.element_size()
+    if out is None:
+        dev = xa.device
+        out = tuple(torch.empty(n, dtype=torch.float32, device=dev) for n in (Nq, Nkv, Nkv, K))
+    Yq, Yk, Yv, Y = out
+    wsp, wsb = _ws(ws)
+    _check(load().bqg_decode_layer_q4_0_q8_1(_dev(xa, "xa", numel=nx), _dev(xb, "xb", numel=nx), dt,
+                                             _dev(Wq, "Wq"), _dev(Wk, "Wk"), _dev(Wv, "Wv"), _dev(Wg, "Wg"),
+                                             _dev(Wu, "Wu"), _dev(Wd, "Wd"),
+                                             _dev(Yq, "Yq", torch.float32, Nq * 4), _dev(Yk, "Yk", torch.float32, Nkv * 4),
+                                             _dev(Yv, "Yv", torch.float32, Nkv * 4), _dev(Y, "Y", torch.float32, K * 4),
+                                             1, Nq, Nkv, Nff, K, wsp, wsb, _stream(stream)),
+           "bqg_decode_layer_q4_0_q8_1")
+    return out
+
+
+def layer_hq(ws, Nff):
+    """The q8_1 blocks of h (uint8, Nff/32 * 36) inside a decode-layer workspace."""
+    up16 = lambda b: (b + 15) // 16 * 16
+    off = up16(Nff * 4) + up16(Nff // QK * 4)
+    return ws[off:off + Nff // QK * BLOCK_BYTES[Q8_1]]
 
 
 def gemm_q4_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):

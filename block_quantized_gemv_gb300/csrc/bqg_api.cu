@@ -28,6 +28,9 @@ int gemv_x_stage_bytes_bf16(int, int, int);
 int gemv_x_stage_bytes_q8_0(int, int, int);
 int gemv_x_stage_bytes_q4_0(int, int, int);
 int gemv_x_stage_bytes_q4_0_q8_1(int, int, int);
+cudaError_t layer_occupancy(int threads, size_t smem, int *bpsm);
+cudaError_t layer_launch(const LayerParams &lp, int grid, int threads, size_t smem, cudaStream_t stream);
+cudaError_t layer_take_error(int *out);
 cudaError_t launch_quantize_q8_1(const void *, int, void *, int, int64_t, cudaStream_t, bool);
 cudaError_t launch_rmsnorm_q8_1(const void *, int, const float *, float, void *, int, int64_t, cudaStream_t, bool);
 cudaError_t launch_quantize_weights(int, const float *, void *, int64_t, int64_t, cudaStream_t);
@@ -465,6 +468,24 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     return BQG_OK;
 }
 
+// Workspace of the persistent decode layer (Nff = rows of gate and of up):
+// fp32 h staging, one arrival counter per q8_1 block of h, the q8_1 blocks
+// of h, then the two grid-barrier words (16-byte aligned parts).
+struct LayerWs {
+    size_t h, cnt, hq, gbar, total;
+};
+LayerWs layer_ws(int64_t Nff)
+{
+    auto up16 = [](size_t b) { return (b + 15) / 16 * 16; };
+    LayerWs w;
+    w.h = 0;
+    w.cnt = up16((size_t)Nff * 4);
+    w.hq = w.cnt + up16((size_t)(Nff / QK) * 4);
+    w.gbar = w.hq + up16((size_t)(Nff / QK) * Q8_1_BYTES);
+    w.total = w.gbar + 16;
+    return w;
+}
+
 int check_k(int64_t K)
 {
     if (K <= 0 || K % QK) return BQG_ERR_UNSUPPORTED_SHAPE;
@@ -645,6 +666,97 @@ int bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(const void *Wg, const void *Wu, const
     return run_gemv(W_Q4_0, X_Q8_1, p, M, K, EPI_SWIGLU, ws, ws_bytes, stream, (uint8_t *)Hq);
 }
 
+int bqg_decode_layer_q4_0_q8_1(const void *xa, const void *xb, int x_dtype, const void *Wq, const void *Wk,
+                               const void *Wv, const void *Wg, const void *Wu, const void *Wd, float *Yq, float *Yk,
+                               float *Yv, float *Y, int M, int64_t Nq, int64_t Nkv, int64_t Nff, int64_t K, void *ws,
+                               size_t ws_bytes, cudaStream_t stream)
+{
+    if (!xa || !xb || !Wq || !Wk || !Wv || !Wg || !Wu || !Wd || !Yq || !Yk || !Yv || !Y || !ws)
+        return BQG_ERR_INVALID_ARG;
+    if (Nq <= 0 || Nkv <= 0 || Nff <= 0 || (x_dtype != BQG_BF16 && x_dtype != BQG_F32)) return BQG_ERR_INVALID_ARG;
+    if (M != 1) return BQG_ERR_UNSUPPORTED_SHAPE;
+    if (int st = check_k(K)) return st;
+    if (int st = check_k(Nff)) return st;
+    const bool f32 = (x_dtype == BQG_F32);
+    if (!aligned16(Wq) || !aligned16(Wk) || !aligned16(Wv) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) ||
+        !aligned16(ws) || !aligned(xa, f32 ? 4 : 2) || !aligned(xb, f32 ? 4 : 2) || !aligned(Yq, 4) ||
+        !aligned(Yk, 4) || !aligned(Yv, 4) || !aligned(Y, 4))
+        return BQG_ERR_MISALIGNED;
+    const LayerWs w = layer_ws(Nff);
+    if (ws_bytes < w.total) return BQG_ERR_WORKSPACE;
+    DevInfo dev;
+    if (int st = current_device(&dev)) return st;
+
+    // shared memory: one slot per warp (the larger stage of the two phases),
+    // staged activations (the larger phase), phase 1's q8_1 blocks, barriers
+    constexpr int NW = 12, RL1 = 2, RL2 = 1;
+    const int64_t rb1 = repacked_row_bytes(BQG_Q4_0, K), rb2 = repacked_row_bytes(BQG_Q4_0, Nff);
+    const int nb1 = (int)(K / QK), nb2 = (int)(Nff / QK);
+    const int nc1 = chunk_space(W_Q4_0, K), nc2 = chunk_space(W_Q4_0, Nff);
+    const int xrb1 = (x_stage_bytes(W_Q4_0, X_Q8_1, nc1, nb1, 0) + 15) / 16 * 16;
+    const int xrb2 = (x_stage_bytes(W_Q4_0, X_Q8_1, nc2, nb2, 0) + 15) / 16 * 16;
+    LayerParams lp{};
+    lp.slot_bytes = (int)std::max<int64_t>(RL1 * rb1, RL2 * rb2);
+    lp.x_off = NW * lp.slot_bytes;
+    lp.xraw_off = lp.x_off + std::max(xrb1, xrb2);
+    lp.bar_off = lp.xraw_off + (std::max(nb1, nb2) * Q8_1_BYTES + 15) / 16 * 16;
+    const size_t smem = (size_t)lp.bar_off + 8 * (NW + 1);
+    if (smem > 232448) return BQG_ERR_UNSUPPORTED_SHAPE;
+    int bpsm = 0;
+    if (cudaError_t e = layer_occupancy(32 * NW, smem, &bpsm)) return cuda_status(e);
+    bpsm = std::min(bpsm, 2);
+    if (bpsm < 1) return BQG_ERR_UNSUPPORTED_SHAPE;
+    const int grid = dev.sms * bpsm;
+    // phase 1's CTAs split between qkv and gate/up in proportion to their bytes
+    const double qb = (double)(Nq + 2 * Nkv), gb = (double)(2 * Nff);
+    lp.cq = (int)std::min<int64_t>(grid - 1, std::max<int64_t>(1, (int64_t)(grid * qb / (qb + gb) + 0.5)));
+
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    GemvParams &a = lp.qkv;
+    a.W[0] = (const uint8_t *)Wq; a.W[1] = (const uint8_t *)Wk; a.W[2] = (const uint8_t *)Wv;
+    a.Y[0] = Yq; a.Y[1] = Yk; a.Y[2] = Yv;
+    a.rows[0] = Nq; a.rows[1] = Nkv; a.rows[2] = Nkv;
+    a.nmat = 3;
+    a.Nv = Nq + 2 * Nkv;
+    GemvParams &g = lp.gu;
+    g.W[0] = (const uint8_t *)Wg; g.W[1] = (const uint8_t *)Wu;
+    g.Y[0] = reinterpret_cast<float *>(wsb + w.h);
+    g.rows[0] = Nff; g.rows[1] = Nff;
+    g.nmat = 2;
+    g.Nv = 2 * Nff;
+    g.hq = wsb + w.hq;
+    g.cnt = reinterpret_cast<int *>(wsb + w.cnt);
+    for (GemvParams *q : {&a, &g}) {
+        q->epi = (q == &g) ? EPI_SWIGLU : EPI_STORE;
+        q->row_bytes = rb1;
+        q->row_stride = (int)rb1;
+        q->K = (int)K;
+        q->nb = nb1;
+        q->nc = nc1;
+        q->x_row_bytes = xrb1;
+    }
+    GemvParams &d = lp.dn;
+    d.W[0] = (const uint8_t *)Wd;
+    d.Y[0] = Y;
+    d.rows[0] = K;
+    d.nmat = 1;
+    d.Nv = K;
+    d.epi = EPI_STORE;
+    d.X = wsb + w.hq;
+    d.row_bytes = rb2;
+    d.row_stride = (int)rb2;
+    d.K = (int)Nff;
+    d.nb = nb2;
+    d.nc = nc2;
+    d.x_row_bytes = xrb2;
+    lp.xa = xa;
+    lp.xb = xb;
+    lp.x_f32 = f32 ? 1 : 0;
+    lp.gbar = reinterpret_cast<unsigned long long *>(wsb + w.gbar);
+    if (cudaError_t e = layer_launch(lp, grid, 32 * NW, smem, stream)) return cuda_status(e);
+    return BQG_OK;
+}
+
 static int gemm_entry(int fmt, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, void *ws,
                       size_t ws_bytes, cudaStream_t stream)
 {
@@ -686,6 +798,7 @@ size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K)
 {
     if (N <= 0 || K <= 0 || K % QK || K > kMaxK) return 0;
     if (op == BQG_OP_GEMM_Q4_0_BF16 || op == BQG_OP_GEMM_Q8_0_BF16) return gemm_workspace(M, N, K);
+    if (op == BQG_OP_DECODE_LAYER_Q4_0_Q8_1) return (M == 1 && N % QK == 0 && N <= kMaxK) ? layer_ws(N).total : 0;
     if (!valid_m(M)) return 0;
     DevInfo dev;
     int dv = 0;
@@ -715,7 +828,7 @@ int bqg_last_device_error(cudaStream_t stream, int *out)
     int word = 0;
     if (int st = gemm_read_error(stream, &word)) return st;
     int w = 0;
-    for (auto fn : {gemv_error_bf16, gemv_error_q8_0, gemv_error_q4_0, gemv_error_q4_0_q8_1}) {
+    for (auto fn : {gemv_error_bf16, gemv_error_q8_0, gemv_error_q4_0, gemv_error_q4_0_q8_1, layer_take_error}) {
         if (fn(&w) != cudaSuccess) return BQG_ERR_CUDA;
         word |= w;
     }

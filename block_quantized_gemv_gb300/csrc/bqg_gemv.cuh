@@ -83,6 +83,22 @@ struct GemvParams {
     int *cnt;
 };
 
+// One decode layer's three projection groups in one persistent launch
+// (bqg_layer.cu; the entry point validates and plans it).
+struct LayerParams {
+    GemvParams qkv;         // phase 1, CTAs [0, cq): nmat 3, whole rows, K = model width
+    GemvParams gu;          // phase 1, CTAs [cq, grid): nmat 2 (gate/up interleaved), SwiGLU -> q8_1
+    GemvParams dn;          // phase 2, every CTA: nmat 1, K = Nff, activations = gu.hq
+    const void *xa, *xb;    // activation rows of qkv and gate/up (K values each)
+    int x_f32;              // activations fp32 (else bf16)
+    int cq;                 // phase-1 CTAs given to qkv
+    int slot_bytes;         // per-warp slot (largest stage of the two phases)
+    int x_off;              // staged activations (room for the larger phase)
+    int xraw_off;           // phase 1's q8_1 blocks before staging
+    int bar_off;            // one mbarrier per warp
+    unsigned long long *gbar;   // grid barrier word in the workspace: generation << 32 | arrivals
+};
+
 // Error word set when a bounded wait gives up (one per translation unit).
 static __device__ int g_gemv_error;
 

@@ -86,7 +86,8 @@ enum {
     BQG_OP_GATE_UP_Q4_0_Q8_1 = 5,   /* N = rows of each of gate and up */
     BQG_OP_GEMM_Q4_0_BF16 = 6,
     BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1 = 7, /* gate+up SwiGLU with q8_1 output; N = rows of each */
-    BQG_OP_GEMM_Q8_0_BF16 = 8
+    BQG_OP_GEMM_Q8_0_BF16 = 8,
+    BQG_OP_DECODE_LAYER_Q4_0_Q8_1 = 9  /* M = 1; N = Nff (rows of each of gate and up), K = model width */
 };
 
 /* ---- load time ------------------------------------------------------- */
@@ -208,6 +209,37 @@ int bqg_gemv_q4_0_q8_1_gate_up_swiglu(const void *Wg, const void *Wu, const void
 int bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(const void *Wg, const void *Wu, const void *Xq, void *Hq, int M,
                                            int64_t N, int64_t K, void *ws, size_t ws_bytes,
                                            cudaStream_t stream);
+
+/* One decode layer's three projection groups in one persistent launch
+ * ("MI50 megakernel", hypothesis ledger: neighbouring steps fused into one
+ * dispatch with a grid-wide barrier between dependent steps; "rx-6700xt-
+ * llama2-decode", Approach & Methodology: the q4_0 x q8_1 matvec and its fused
+ * QKV and gate+up/SwiGLU dispatches).  M = 1.  Computes, as the separate
+ * entry points would:
+ *   xqa = q8_1(xa), xqb = q8_1(xb)              (the rules of bqg_quantize_q8_1)
+ *   Yq, Yk, Yv = Wq . xqa, Wk . xqa, Wv . xqa   (bqg_gemv_q4_0_q8_1_qkv)
+ *   hq = q8_1(silu(Wg . xqb) * (Wu . xqb))      (..._gate_up_swiglu_q8_1)
+ *   Y  = Wd . hq                                (bqg_gemv_q4_0_q8_1)
+ * xa, xb: K values each, x_dtype BQG_BF16 or BQG_F32 (2- or 4-byte aligned).
+ * Wq: Nq x K, Wk and Wv: Nkv x K, Wg and Wu: Nff x K, Wd: K x Nff, all
+ * repacked q4_0 (16-byte aligned).  Yq: Nq, Yk and Yv: Nkv, Y: K fp32.
+ * K and Nff multiples of 32.  The launch is cooperative (every CTA resident
+ * at once, as the grid barrier needs; the runtime refuses it otherwise,
+ * reported as BQG_ERR_CUDA).  ws: bqg_workspace_size(
+ * BQG_OP_DECODE_LAYER_Q4_0_Q8_1, 1, Nff, K) bytes, 16-byte aligned, ZERO
+ * before the first call on it (every successful call leaves its counters
+ * zero; after a BQG_ERR_TIMEOUT report zero it again); it holds h (fp32),
+ * the q8_1 blocks of h, their arrival counters and the grid barrier.  Calls
+ * sharing a workspace must not overlap.  Errors: INVALID_ARG (null pointer,
+ * non-positive size, other x_dtype), UNSUPPORTED_SHAPE (M != 1, K or Nff not
+ * a multiple of 32 or above 65536, stages that do not fit in shared memory),
+ * MISALIGNED, WORKSPACE (ws too small); a bounded device wait that gives up
+ * (one stage, or the grid barrier after about a second) is reported by
+ * bqg_last_device_error. */
+int bqg_decode_layer_q4_0_q8_1(const void *xa, const void *xb, int x_dtype, const void *Wq, const void *Wk,
+                               const void *Wv, const void *Wg, const void *Wu, const void *Wd, float *Yq, float *Yk,
+                               float *Yv, float *Y, int M, int64_t Nq, int64_t Nkv, int64_t Nff, int64_t K, void *ws,
+                               size_t ws_bytes, cudaStream_t stream);
 
 /* Prefill GEMM ("llama-3x-prompt-speed", "the tile"): each weight tile is
  * dequantized once to bf16 ((q-8)*d rounded to nearest-even bf16) into the

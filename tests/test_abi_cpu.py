@@ -85,6 +85,15 @@ FAKE = 0x10000  # never dereferenced: every call below fails validation first
     (lambda L: L.bqg_rmsnorm_quantize_q8_1(FAKE, 0, None, 1e-5, FAKE, 1, 40, None), 2),         # K % 32
     (lambda L: L.bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(FAKE, FAKE, FAKE, FAKE, 1, 40, 64, None, 0, None), 2),  # N % 32
     (lambda L: L.bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(FAKE, FAKE, FAKE, FAKE + 2, 1, 64, 64, None, 0, None), 3),
+    # persistent decode layer: (xa, xb, dtype, Wq, Wk, Wv, Wg, Wu, Wd, Yq, Yk, Yv, Y, M, Nq, Nkv, Nff, K, ws, bytes, s)
+    (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 0, *[FAKE] * 10, 1, 64, 64, 128, 64, None, 0, None), 1),   # ws
+    (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 7, *[FAKE] * 10, 1, 64, 64, 128, 64, FAKE, 1 << 20, None), 1),
+    (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 0, *[FAKE] * 10, 2, 64, 64, 128, 64, FAKE, 1 << 20, None), 2),
+    (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 0, *[FAKE] * 10, 1, 64, 64, 120, 64, FAKE, 1 << 20, None), 2),
+    (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 0, *[FAKE] * 10, 1, 64, 0, 128, 64, FAKE, 1 << 20, None), 1),
+    (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 0, FAKE + 8, *[FAKE] * 9, 1, 64, 64, 128, 64, FAKE, 1 << 20,
+                                            None), 3),
+    (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 0, *[FAKE] * 10, 1, 64, 64, 128, 64, FAKE, 64, None), 7),
 ])
 def test_host_validation_rejects_before_launch(L, call, status):
     assert call(L) == status
