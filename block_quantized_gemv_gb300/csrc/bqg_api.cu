@@ -138,6 +138,7 @@ int x_stage_bytes(int wf, int xf, int nc, int nb, int bf16)
 
 struct GemvPlan {
     bool lpr;               // lanes-per-row kernel
+    bool x_bf16s;           // bf16 activations staged as bf16 (M = 1 as well)
     int L, x_off, x_row_bytes, xraw_off, early, rl, piece_chunks, wg, ng;
     int C, TPR, RG, RPS, nc, cps, splits, threads, ncons, S, NS, stride, win_stages, part_off, bar_off, ctas;
     dim3 grid;
@@ -292,10 +293,14 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     g.splits = 1;
     if (Nv < (int64_t)dev.sms * 4)
         g.splits = (int)std::min<int64_t>(maxs, ((int64_t)dev.sms * 4 + Nv - 1) / std::max<int64_t>(Nv, 1));
-    // M = 4, 8 with bf16 activations: rows staged as bf16, copied in place
-    // (no raw copy); else staged rows plus their raw copy (the
-    // 16-byte-aligned span around X: up to 15 bytes of slack on either side)
-    const bool bf16s = (M >= 4 && xf == X_BF16);
+    // bf16 activations at M = 4, 8 (fp32 rows would not fit) and, measured
+    // faster, at M = 1 against quantized weights (half the shared-memory
+    // reads per weight): rows staged as bf16, copied in place (no raw copy);
+    // else staged rows plus their raw copy (the 16-byte-aligned span around
+    // X: up to 15 bytes of slack on either side)
+    static const int bf16x_m1 = env_int("BQG_LPR_BF16X", 1);
+    const bool bf16s = xf == X_BF16 && (M >= 4 || (M == 1 && wf != W_BF16 && bf16x_m1));
+    g.x_bf16s = bf16s;
     g.x_row_bytes = (x_stage_bytes(wf, xf, g.nc, nb, bf16s ? 1 : 0) + 15) / 16 * 16;
     const int xraw = bf16s ? 0 : (int)((M * ((xf == X_Q8_1) ? (int64_t)nb * Q8_1_BYTES : K * 2) + 30) / 16 * 16);
     const int xbytes = M * g.x_row_bytes + xraw + 16;
@@ -313,11 +318,13 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     // consecutive rows (the copy engine costs about as much per copy as per
     // few KiB moved).
     g.L = 32;
-    // measured on the decode shapes: two rows per warp for q4_0 x q8_1 (its
-    // rows are short, so the copy stays large), one row for the others
     // measured on the decode and sweep shapes: two rows per lane for q8_1
     // activations (M = 1, 2) and for q4_0 x bf16 at M = 1, one otherwise
     int rl = ((M <= 2 && xf == X_Q8_1) || (M == 1 && wf == W_Q4_0)) ? 2 : 1;
+    // q8_0 x bf16 at M = 1 (bf16-staged): two rows per lane when each CTA
+    // has few rows (N = 4096: 13 per CTA), one row and two slots otherwise
+    const bool q8_m1_few = bf16x_m1 && M == 1 && wf == W_Q8_0 && xf == X_BF16 && Nv < (int64_t)dev.sms * 2 * 24;
+    if (q8_m1_few) rl = 2;
     if (force_rl == 1 || force_rl == 2 || (force_rl == 4 && M == 1)) rl = force_rl;
     // M = 4, 8 (measured on the sweep shapes): two rows per lane, but one
     // for q8_0 at M = 8, whose dequant registers then spill
@@ -346,7 +353,7 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     // measured: q8_1 activations, q4_0 weights and M >= 2 gain more from
     // more warps with one slot each than from double slots; bf16 and q8_0
     // weights at M = 1 keep two
-    const bool one_slot = xf == X_Q8_1 || M >= 2 || wf == W_Q4_0;
+    const bool one_slot = xf == X_Q8_1 || M >= 2 || wf == W_Q4_0 || q8_m1_few;
     const int want_D = (force_D > 0) ? force_D : one_slot ? 1 : 0;
     if (want_D > 0) { D = want_D; ng = std::max(1, std::min(max_warps, slots / D)); }
     g.ng = ng;
@@ -374,6 +381,7 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
             lk.unlock();
             GemvParams dummy{};
             dummy.rl = g.rl;
+            dummy.x_bf16s = g.x_bf16s ? 1 : 0;
             const cudaError_t e = lpr_runner(wf, xf)(dummy, M, dim3(1), g.threads, g.smem, 0, false, &bpsm);
             if (e != cudaSuccess) return cuda_status(e);
             lk.lock();
@@ -454,6 +462,7 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     p.early = g.early;
     p.rl = g.rl;
     p.piece_chunks = g.piece_chunks;
+    p.x_bf16s = g.x_bf16s ? 1 : 0;
     p.x_row_bytes = g.x_row_bytes;
     p.ws = (g.splits > 1) ? (float *)ws : nullptr;
     p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;

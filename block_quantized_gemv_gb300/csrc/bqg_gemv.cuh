@@ -76,6 +76,7 @@ struct GemvParams {
     int early;              // stages per warp requested before waiting for the previous grid
     int rl;                 // rows per lane (lanes-per-row kernel: 1, 2 or 4)
     int piece_chunks;       // chunks per K-piece (lanes-per-row kernel)
+    int x_bf16s;            // lanes-per-row kernel at M = 1: bf16 activations staged as bf16
     // SwiGLU with a q8_1 output: the blocks go to hq (M x rows[0]/32 blocks);
     // Y[0] is then an fp32 staging row set and cnt one arrival counter per
     // block (zero between calls)
@@ -1345,6 +1346,11 @@ __host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, in
 {
     constexpr int XR = (XF == X_BF16) ? X_F32 : XF;      // M <= 2: bf16 activations staged as fp32
     const int rl = p.rl;
+    if constexpr (XF == X_BF16 && WF != W_BF16) {
+        // M = 1 with bf16-staged activations (half the shared-memory reads, one conversion per use)
+        if (M == 1 && p.x_bf16s && rl == 1) return gemv_lpr_launch_one<WF, X_BF16, 1, 1>(p, grid, threads, smem, stream, pdl, occupancy);
+        if (M == 1 && p.x_bf16s && rl == 2) return gemv_lpr_launch_one<WF, X_BF16, 1, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+    }
     if (M == 1 && rl == 1) return gemv_lpr_launch_one<WF, XR, 1, 1>(p, grid, threads, smem, stream, pdl, occupancy);
     if (M == 1 && rl == 2) return gemv_lpr_launch_one<WF, XR, 1, 2>(p, grid, threads, smem, stream, pdl, occupancy);
     if (M == 1 && rl == 4) return gemv_lpr_launch_one<WF, XR, 1, 4>(p, grid, threads, smem, stream, pdl, occupancy);
