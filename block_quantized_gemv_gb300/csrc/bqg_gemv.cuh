@@ -1350,6 +1350,8 @@ __host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, in
         // M = 1 with bf16-staged activations (half the shared-memory reads, one conversion per use)
         if (M == 1 && p.x_bf16s && rl == 1) return gemv_lpr_launch_one<WF, X_BF16, 1, 1>(p, grid, threads, smem, stream, pdl, occupancy);
         if (M == 1 && p.x_bf16s && rl == 2) return gemv_lpr_launch_one<WF, X_BF16, 1, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+        if (M == 2 && p.x_bf16s && rl == 1) return gemv_lpr_launch_one<WF, X_BF16, 2, 1>(p, grid, threads, smem, stream, pdl, occupancy);
+        if (M == 2 && p.x_bf16s && rl == 2) return gemv_lpr_launch_one<WF, X_BF16, 2, 2>(p, grid, threads, smem, stream, pdl, occupancy);
     }
     if (M == 1 && rl == 1) return gemv_lpr_launch_one<WF, XR, 1, 1>(p, grid, threads, smem, stream, pdl, occupancy);
     if (M == 1 && rl == 2) return gemv_lpr_launch_one<WF, XR, 1, 2>(p, grid, threads, smem, stream, pdl, occupancy);
