@@ -325,7 +325,8 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     // has few rows (N = 4096: 13 per CTA), one row and two slots otherwise
     const bool q8_m1_few = bf16x_m1 && M == 1 && wf == W_Q8_0 && xf == X_BF16 && Nv < (int64_t)dev.sms * 2 * 24;
     if (q8_m1_few) rl = 2;
-    if (force_rl == 1 || force_rl == 2 || (force_rl == 4 && M == 1)) rl = force_rl;
+    // (four rows per lane: instantiated for fp32- or q8_1-staged M = 1 only)
+    if (force_rl == 1 || force_rl == 2 || (force_rl == 4 && M == 1 && !bf16s)) rl = force_rl;
     // M = 4, 8 (measured on the sweep shapes): two rows per lane, but one
     // for q8_0 at M = 8, whose dequant registers then spill
     if (force_rl == 0 && M >= 4) rl = (wf == W_Q8_0 && M == 8) ? 1 : 2;

@@ -1344,25 +1344,26 @@ template <int WF, int XF>
 __host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, int threads, size_t smem,
                                        cudaStream_t stream, bool pdl, int *occupancy)
 {
-    constexpr int XR = (XF == X_BF16) ? X_F32 : XF;      // M <= 2: bf16 activations staged as fp32
+    // The staging the plan chose (bf16 pieces, fp32, or q8_1) selects the
+    // instantiation; a combination without one is an error, never a kernel
+    // that expects another staging.
     const int rl = p.rl;
-    if constexpr (XF == X_BF16 && WF != W_BF16) {
-        // M = 1 with bf16-staged activations (half the shared-memory reads, one conversion per use)
-        if (M == 1 && p.x_bf16s && rl == 1) return gemv_lpr_launch_one<WF, X_BF16, 1, 1>(p, grid, threads, smem, stream, pdl, occupancy);
-        if (M == 1 && p.x_bf16s && rl == 2) return gemv_lpr_launch_one<WF, X_BF16, 1, 2>(p, grid, threads, smem, stream, pdl, occupancy);
-        if (M == 2 && p.x_bf16s && rl == 1) return gemv_lpr_launch_one<WF, X_BF16, 2, 1>(p, grid, threads, smem, stream, pdl, occupancy);
-        if (M == 2 && p.x_bf16s && rl == 2) return gemv_lpr_launch_one<WF, X_BF16, 2, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+#define BQG_LPR(XX, MM, RR) \
+    if (M == MM && rl == RR) return gemv_lpr_launch_one<WF, XX, MM, RR>(p, grid, threads, smem, stream, pdl, occupancy);
+    if constexpr (XF == X_BF16) {
+        if (p.x_bf16s) {
+            if constexpr (WF != W_BF16) {
+                BQG_LPR(X_BF16, 1, 1) BQG_LPR(X_BF16, 1, 2) BQG_LPR(X_BF16, 2, 1) BQG_LPR(X_BF16, 2, 2)
+            }
+            BQG_LPR(X_BF16, 4, 1) BQG_LPR(X_BF16, 4, 2) BQG_LPR(X_BF16, 8, 1) BQG_LPR(X_BF16, 8, 2)
+            return cudaErrorInvalidValue;
+        }
+        BQG_LPR(X_F32, 1, 1) BQG_LPR(X_F32, 1, 2) BQG_LPR(X_F32, 1, 4) BQG_LPR(X_F32, 2, 1) BQG_LPR(X_F32, 2, 2)
+    } else {
+        BQG_LPR(XF, 1, 1) BQG_LPR(XF, 1, 2) BQG_LPR(XF, 1, 4) BQG_LPR(XF, 2, 1) BQG_LPR(XF, 2, 2)
+        BQG_LPR(XF, 4, 1) BQG_LPR(XF, 4, 2) BQG_LPR(XF, 8, 1) BQG_LPR(XF, 8, 2)
     }
-    if (M == 1 && rl == 1) return gemv_lpr_launch_one<WF, XR, 1, 1>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 1 && rl == 2) return gemv_lpr_launch_one<WF, XR, 1, 2>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 1 && rl == 4) return gemv_lpr_launch_one<WF, XR, 1, 4>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 2 && rl == 1) return gemv_lpr_launch_one<WF, XR, 2, 1>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 2 && rl == 2) return gemv_lpr_launch_one<WF, XR, 2, 2>(p, grid, threads, smem, stream, pdl, occupancy);
-    // M = 4, 8: bf16 activations staged as bf16
-    if (M == 4 && rl == 1) return gemv_lpr_launch_one<WF, XF, 4, 1>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 4 && rl == 2) return gemv_lpr_launch_one<WF, XF, 4, 2>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 8 && rl == 1) return gemv_lpr_launch_one<WF, XF, 8, 1>(p, grid, threads, smem, stream, pdl, occupancy);
-    if (M == 8 && rl == 2) return gemv_lpr_launch_one<WF, XF, 8, 2>(p, grid, threads, smem, stream, pdl, occupancy);
+#undef BQG_LPR
     return cudaErrorInvalidValue;
 }
 
