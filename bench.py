@@ -231,6 +231,34 @@ class GemvArm(Arm):
         return 2 * self.M * self.N * self.K
 
 
+class VendorGemvArm(Arm):
+    """Context arm, not this library: torch.matmul (cuBLAS) bf16 y = x W^T at the
+    same shape, rotation and timing as the bf16 GEMV arm (bf16 output, as the
+    library call returns).  Its launches are not counted as ours."""
+    vendor = True
+    launches_per_call = 0
+
+    def __init__(self, M=1, N=12288, K=4096, seed=1):
+        import torch
+        from block_quantized_gemv_gb300 import synth
+        super().__init__()
+        self.M, self.N, self.K = M, N, K
+        self.name = f"vendor arm: torch.matmul (cuBLAS) bf16 GEMV M={M} K={K} N={N}"
+        self.kernel_key = ""
+        W = torch.from_numpy(synth.weights_f32(N, K, seed)).cuda().to(torch.bfloat16)
+        x = torch.from_numpy(synth.activations_f32(M, K, seed + 1)).cuda().to(torch.bfloat16)
+        self.bytes_per_call = N * K * 2 + M * K * 2 + M * N * 2
+        self.R = self.rotation(self.bytes_per_call)
+        for r in range(self.R):
+            self.sets.append({"W": W if r == 0 else W.clone(), "x": x.clone(),
+                              "y": torch.empty((M, N), dtype=torch.bfloat16, device="cuda")})
+
+    def call(self, i):
+        import torch
+        s = self.sets[i % self.R]
+        torch.matmul(s["x"], s["W"].t(), out=s["y"])
+
+
 class GemmArm(Arm):
     """Prefill GEMM M=512 (bf16 activations) x q4_0 (or q8_0) weights."""
 
@@ -438,6 +466,8 @@ def arm_record(arm, t, peaks):
            "rotating_sets": arm.R, "working_set_bytes": arm.R * arm.bytes_per_call,
            "spread": round(t["spread"], 4), "spread_ok": t["spread_ok"],
            "launches": calls * arm.launches_per_call}
+    if getattr(arm, "vendor", False):
+        rec["vendor"] = "library GEMV for context (cuBLAS through torch.matmul), not this repository's kernels"
     if getattr(arm, "flops", None):
         tf = arm.flops * calls / t["seconds"] / 1e12
         rec.update({"bound": "tensor", "TFLOP_per_s": round(tf, 1),
@@ -584,7 +614,7 @@ def main():
 
     arms = [rec]
     other = [GemvArm(bqg.Q8_0, bqg.BF16, 1, N_HEAD, K_HEAD), GemvArm(bqg.Q4_0, bqg.Q8_1, 1, N_HEAD, K_HEAD),
-             GemmArm()]
+             GemmArm(), VendorGemvArm(1, N_HEAD, K_HEAD)]
     if args.suite == "full":
         other += [GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096), DecodeLayerArm(), DecodeLayerArm(fused_norm=True),
                   DecodeLayerArm(persistent=True),
