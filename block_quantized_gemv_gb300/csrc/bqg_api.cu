@@ -294,12 +294,12 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     if (Nv < (int64_t)dev.sms * 4)
         g.splits = (int)std::min<int64_t>(maxs, ((int64_t)dev.sms * 4 + Nv - 1) / std::max<int64_t>(Nv, 1));
     // bf16 activations at M = 4, 8 (fp32 rows would not fit) and, measured
-    // faster, at M = 1, 2 against quantized weights (half the shared-memory
+    // faster for every weight format, at M = 1, 2 (half the shared-memory
     // reads per weight): rows staged as bf16, copied in place (no raw copy);
     // else staged rows plus their raw copy (the 16-byte-aligned span around
     // X: up to 15 bytes of slack on either side)
     static const int bf16x_m1 = env_int("BQG_LPR_BF16X", 1);
-    const bool bf16s = xf == X_BF16 && (M >= 4 || (wf != W_BF16 && bf16x_m1));
+    const bool bf16s = xf == X_BF16 && (M >= 4 || bf16x_m1);
     g.x_bf16s = bf16s;
     g.x_row_bytes = (x_stage_bytes(wf, xf, g.nc, nb, bf16s ? 1 : 0) + 15) / 16 * 16;
     const int xraw = bf16s ? 0 : (int)((M * ((xf == X_Q8_1) ? (int64_t)nb * Q8_1_BYTES : K * 2) + 30) / 16 * 16);
@@ -318,9 +318,10 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     // consecutive rows (the copy engine costs about as much per copy as per
     // few KiB moved).
     g.L = 32;
-    // measured on the decode and sweep shapes: two rows per lane for q8_1
-    // activations and for q4_0 x bf16 (M = 1, 2), one otherwise
-    int rl = (M <= 2 && wf == W_Q4_0) ? 2 : 1;
+    // measured on the decode and sweep shapes: two rows per lane for q4_0
+    // (q8_1 or bf16 activations) at M = 1, 2 and for bf16 weights at M = 2,
+    // one otherwise
+    int rl = ((M <= 2 && wf == W_Q4_0) || (M == 2 && wf == W_BF16)) ? 2 : 1;
     // q8_0 x bf16 at M = 1 (bf16-staged): two rows per lane when each CTA
     // has few rows (N = 4096: 13 per CTA), one row and two slots otherwise
     const bool q8_m1_few = bf16x_m1 && M == 1 && wf == W_Q8_0 && xf == X_BF16 && Nv < (int64_t)dev.sms * 2 * 24;

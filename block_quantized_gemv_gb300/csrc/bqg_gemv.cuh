@@ -1352,9 +1352,7 @@ __host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, in
     if (M == MM && rl == RR) return gemv_lpr_launch_one<WF, XX, MM, RR>(p, grid, threads, smem, stream, pdl, occupancy);
     if constexpr (XF == X_BF16) {
         if (p.x_bf16s) {
-            if constexpr (WF != W_BF16) {
-                BQG_LPR(X_BF16, 1, 1) BQG_LPR(X_BF16, 1, 2) BQG_LPR(X_BF16, 2, 1) BQG_LPR(X_BF16, 2, 2)
-            }
+            BQG_LPR(X_BF16, 1, 1) BQG_LPR(X_BF16, 1, 2) BQG_LPR(X_BF16, 2, 1) BQG_LPR(X_BF16, 2, 2)
             BQG_LPR(X_BF16, 4, 1) BQG_LPR(X_BF16, 4, 2) BQG_LPR(X_BF16, 8, 1) BQG_LPR(X_BF16, 8, 2)
             return cudaErrorInvalidValue;
         }
