@@ -680,9 +680,9 @@ __global__ void __launch_bounds__(544, (M == 1) ? 2 : 1) gemv_kernel(const GemvP
 // Staged activations for the lanes-per-row kernel.  Chunk c of activation
 // row m is P pieces of 16 bytes; piece p of chunks 32u .. 32u+31 is one run
 // of 512 bytes, so lanes reading consecutive chunks hit distinct banks.
-// Pieces hold four fp32 (M <= 2) or eight bf16 (X_BF16: M = 4, 8, where
-// fp32 rows would not fit beside the weight stages).  q8_1 rows add, per
-// block, (d as float, exact sum of codes) after the runs.
+// Pieces hold eight bf16 (X_BF16, the default for bf16 activations) or four
+// fp32 (X_F32, bf16 activations at M <= 2 when bf16 staging is off).  q8_1
+// rows add, per block, (d as float, exact sum of codes) after the runs.
 // ---------------------------------------------------------------------------
 template <int WF, int XF> struct XPieces {
     static constexpr int P = ChunkTraits<WF>::E / ((XF == X_BF16) ? 8 : 4);
@@ -697,7 +697,7 @@ __host__ __device__ __forceinline__ int x_stage_row_bytes(int nc, int nb)
 }
 
 // Bytes of one activation row as the caller passes it: q8_1 blocks, or bf16
-// (staged as fp32).
+// (staged as bf16 or fp32).
 template <int XF>
 __device__ __forceinline__ int64_t x_src_row_bytes(const GemvParams &p)
 {
