@@ -106,3 +106,37 @@ def test_decode_layer_rejects_small_workspace():
                                    torch.zeros((1, K), dtype=torch.bfloat16, device="cuda"),
                                    *[z] * 6, Nq, Nq, Nff, K, ws=z)
     assert e.value.status == 7
+
+
+def test_decode_layer_barrier_timeout_is_reported_and_recoverable(ora):
+    """The grid barrier's bounded wait, made to run out without any fault: the
+    workspace's arrival count is preset (against the zero-workspace contract)
+    so that no arrival can ever complete the barrier.  Every CTA gives up
+    after about a second, sets the error word, drains its copies and exits;
+    the host reads the error, and after the workspace is zeroed again the
+    same context computes the layer correctly."""
+    K, Nq, Nkv, Nff = 1024, 256, 64, 512
+    up16 = lambda b: (b + 15) // 16 * 16
+    gbar = up16(Nff * 4) + up16(Nff // 32 * 4) + up16(Nff // 32 * 36)
+    shapes = {"q": (Nq, K), "k": (Nkv, K), "v": (Nkv, K), "g": (Nff, K), "u": (Nff, K), "d": (K, Nff)}
+    canon = {k: make_weights(ora, Q4_0, n, kk, seed=90 + i)[1] for i, (k, (n, kk)) in enumerate(shapes.items())}
+    Wp = {k: gpu_repacked(Q4_0, canon[k], *shapes[k]) for k in canon}
+    x = synth.bf16_tensor(synth.bf16_bits(synth.rms_normalised_f32(1, K, seed=99)))
+    ws = bqg.workspace(bqg.OP_DECODE_LAYER_Q4_0_Q8_1, 1, Nff, K)
+    assert bqg.last_device_error() == 0
+    ws[gbar:gbar + 4] = torch.tensor([0xff, 0xff, 0xff, 0x7f], dtype=torch.uint8, device="cuda")
+    args = (x, x, Wp["q"], Wp["k"], Wp["v"], Wp["g"], Wp["u"], Wp["d"], Nq, Nkv, Nff, K)
+    bqg.decode_layer_q4_0_q8_1(*args, ws=ws)
+    torch.cuda.synchronize()
+    assert bqg.last_device_error() != 0
+    assert bqg.last_device_error() == 0            # read and cleared
+    ws.zero_()
+    Yq, Yk, Yv, Y = bqg.decode_layer_q4_0_q8_1(*args, ws=ws)
+    torch.cuda.synchronize()
+    assert bqg.last_device_error() == 0
+    xq = ora.quantize(Q8_1, x.float().cpu().numpy())
+    Yr, Ar = ora.gemv(Q4_0, canon["q"], Q8_1, xq, 1, Nq, K, nthreads=16)
+    check_close(Yq.view(1, -1), Yr, Ar, "layer q after a barrier timeout")
+    hq = bqg.layer_hq(ws, Nff).cpu().numpy().copy()
+    Yr, Ar = ora.gemv(Q4_0, canon["d"], Q8_1, hq, 1, K, Nff, nthreads=16)
+    check_close(Y.view(1, -1), Yr, Ar, "layer down after a barrier timeout")
