@@ -1,23 +1,27 @@
-// bqg_gemv.cuh -- the skinny-GEMV kernel template (M = 1, 2, 4, 8).
+// bqg_gemv.cuh -- the skinny-GEMV kernels (M = 1, 2, 4, 8).
 //
 // Y[m, n] = sum_k W[n, k] X[m, k] for the memory-bound decode shape of
 // "The Shape That Actually Matters" (M = 1, K = 4096, N = 12288 and the
 // rest of the decode projections).  Design for sm_103a:
 //
-//  * Weights are the only large stream.  They are read once, with 128-bit
-//    non-allocating loads from the repacked layout (include/bqgemv.h), so
-//    every warp-wide load instruction covers 512 contiguous bytes and the
-//    fp16 scales come from the same tile ("Rounds 1-3" of that page: the
-//    layout and the load width, not the byte count, decided the bandwidth).
-//  * Each thread owns a fixed slice of K ("chunks") for every row it
-//    visits, so its slice of the activation rows is loaded into registers
-//    once per CTA and never re-read ("MI50 megakernel", microbenchmark
-//    ladder: re-loading the activation was three of five memory
-//    instructions per iteration).
-//  * A row group of TPR threads covers one row's K range; RB rows are in
-//    flight per thread, so one warp-wide reduction (recursive halving, one
-//    shuffle per value) serves RB*M outputs; groups of more than one warp
-//    finish through shared memory and a named barrier.
+//  * Weights are the only large stream.  They are read once from the
+//    repacked layout (include/bqgemv.h): runs of whole consecutive rows are
+//    single cp.async.bulk copies into shared memory, and inside a tile lane
+//    s of a warp owns block (or 16-byte chunk) s, so every warp-wide shared
+//    load covers 512 contiguous bytes and a block's fp16 scale sits in the
+//    same tile ("Rounds 1-3" of that page: the layout and the load width,
+//    not the byte count, decided the bandwidth).
+//  * The activation rows are staged once per CTA in shared memory, in the
+//    same per-lane layout, so every activation load serves the RL rows a
+//    warp works on ("MI50 megakernel", microbenchmark ladder: re-loading the
+//    activation was three of five memory instructions per iteration).
+//  * gemv_lpr_kernel (the lanes-per-row kernel, every M): each warp streams
+//    its own groups of RL rows through its own shared-memory slots, all 32
+//    lanes on each row, one warp shuffle reduction per output; no producer
+//    warp and no cross-warp coupling.
+//  * gemv_kernel (the K-slice kernel): each thread owns a fixed slice of K
+//    held in registers; serves the shapes whose staged activations would
+//    not fit beside the weight stages.
 //  * Each CTA owns a contiguous range of rows; the grid is sized from the
 //    SM count and the measured occupancy.  Split-K (grid.y > 1) writes
 //    partial sums to a workspace reduced by gemv_splitk_reduce.
