@@ -70,6 +70,8 @@ class BqgError(RuntimeError):
 def load(path: str | None = None) -> ctypes.CDLL:
     """Load (once) and return the shared library; raises if it is not built."""
     global _lib
+    if _lib is not None and path is None:
+        return _lib
     with _lock:
         if _lib is None:
             p = path or LIB_PATH
@@ -98,9 +100,18 @@ def _check(status: int, where: str):
         raise BqgError(status, where)
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream(stream=None) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    """The stream handle to enqueue on: `stream`, else torch's current stream
+    of the current device (read without building a Stream object)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and _cur_device is not None:
+        return _raw_stream(_cur_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None, numel=None):
@@ -110,16 +121,15 @@ def _dev(t: torch.Tensor, name: str, dtype=None, numel=None):
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if numel is not None and t.numel() * t.element_size() < numel:
-        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, needs {numel}")
+    if numel is not None and t.nbytes < numel:
+        raise ValueError(f"{name} holds {t.nbytes} bytes, needs {numel}")
     return t.data_ptr()
 
 
 def _ws(ws):
     if ws is None:
         return None, 0
-    _dev(ws, "ws")
-    return ws.data_ptr(), ws.numel() * ws.element_size()
+    return _dev(ws, "ws"), ws.nbytes
 
 
 def row_bytes(fmt: int, K: int) -> int:
