@@ -222,6 +222,16 @@ class GemvArm(Arm):
         self.fn(s["W"], s["X"], self.N, self.K, out=s["Y"], ws=s["ws"])
 
     def call_e2e(self, i):
+        """One step from pinned host memory to pinned host memory: the SMs
+        pull x over the CPU-GPU link into this set's device buffer
+        (bqg_copy_sm), and the GEMV writes y straight into the pinned host
+        buffer (its host alias)."""
+        s = self.sets[i % self.R]
+        self.bqg.copy_sm(s["X"], self.X_host)
+        self.fn(s["W"], s["X"], self.N, self.K, out=self.Y_host, ws=s["ws"])
+
+    def call_e2e_copy_engine(self, i):
+        """The same step with copy-engine transfers (torch copies) on both sides."""
         s = self.sets[i % self.R]
         s["X"].copy_(self.X_host, non_blocking=True)
         self.fn(s["W"], s["X"], self.N, self.K, out=s["Y"], ws=s["ws"])
@@ -437,17 +447,18 @@ def time_arm(arm, steps, warmup, use_graph=True, min_warm_s=1.0, sampler=None, d
             "spread": spread, "spread_ok": spread < 0.05, "graph": graph is not None}
 
 
-def time_e2e(arm, steps):
+def time_e2e(arm, steps, step_fn=None):
     import torch
+    step = step_fn or arm.call_e2e
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for i in range(3):
-            arm.call_e2e(i)
+            step(i)
         stream.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for i in range(steps):
-            arm.call_e2e(i)
+            step(i)
         b.record(stream)
         stream.synchronize()
     return a.elapsed_time(b) / 1e3
@@ -607,10 +618,16 @@ def main():
     clocks = sampler.summary()
 
     e2e_s = time_e2e(head, args.steps)
+    ce_s = time_e2e(head, args.steps, head.call_e2e_copy_engine)
     e2e = {"value": round(gb_s(head.bytes_per_call * args.steps, e2e_s), 1), "unit": "GB/s",
            "h2d_bytes_per_step": head.x_bytes, "d2h_bytes_per_step": head.y_bytes,
            "us_per_step": round(e2e_s / args.steps * 1e6, 3),
-           "path": "pinned host x -> device, bqg_gemv_bf16 through the Python binding, y -> pinned host"}
+           "path": "through the Python binding, every step: x from pinned host memory into device memory by "
+                   "bqg_copy_sm (SM loads over the CPU-GPU link), bqg_gemv_bf16 writing y straight into pinned "
+                   "host memory (bqg_host_alias); the host reads y there after the final synchronize",
+           "copy_engine": {"value": round(gb_s(head.bytes_per_call * args.steps, ce_s), 1), "unit": "GB/s",
+                           "us_per_step": round(ce_s / args.steps * 1e6, 3),
+                           "path": "the same step with torch copies (copy-engine transfers) of x in and y out"}}
 
     arms = [rec]
     other = [GemvArm(bqg.Q8_0, bqg.BF16, 1, N_HEAD, K_HEAD), GemvArm(bqg.Q4_0, bqg.Q8_1, 1, N_HEAD, K_HEAD),

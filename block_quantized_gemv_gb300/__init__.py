@@ -47,6 +47,8 @@ EXPORTS = {
     "bqg_workspace_size": (["i", "i", "i64", "i64"], "size"),
     "bqg_last_device_error": (["p", "p"], "i"),
     "bqg_set_pdl": (["i"], "i"),
+    "bqg_host_alias": (["p", "p"], "i"),
+    "bqg_copy_sm": (["p", "p", "size", "p"], "i"),
     "bqg_status_string": (["i"], "str"),
     "bqg_version": ([], "str"),
     "bqg_last_cuda_error": ([], "str"),
@@ -126,6 +128,38 @@ def _dev(t: torch.Tensor, name: str, dtype=None, numel=None):
     return t.data_ptr()
 
 
+def host_alias(t: torch.Tensor) -> int:
+    """Device-side address of a page-locked (pinned) CPU tensor's memory:
+    kernels given it read or write host memory over the CPU-GPU link."""
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("host_alias wants a pinned CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError("the tensor must be contiguous")
+    out = ctypes.c_void_p(0)
+    _check(load().bqg_host_alias(t.data_ptr(), ctypes.addressof(out)), "bqg_host_alias")
+    return out.value
+
+
+def _dev_or_host(t: torch.Tensor, name: str, dtype=None, numel=None):
+    """_dev for a CUDA tensor; the host alias for a pinned CPU tensor."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if numel is not None and t.nbytes < numel:
+            raise ValueError(f"{name} holds {t.nbytes} bytes, needs {numel}")
+        return host_alias(t)
+    return _dev(t, name, dtype, numel)
+
+
+def copy_sm(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """Copy src's bytes into dst with a kernel instead of a copy engine; each
+    of the two may be a CUDA tensor or a pinned CPU tensor."""
+    n = src.nbytes
+    _check(load().bqg_copy_sm(_dev_or_host(dst, "dst", numel=n), _dev_or_host(src, "src"), n, _stream(stream)),
+           "bqg_copy_sm")
+    return dst
+
+
 def _ws(ws):
     if ws is None:
         return None, 0
@@ -200,7 +234,8 @@ def _gemv(fn: str, Wp, X, N: int, K: int, M: int, out, ws, stream, xbytes):
         out = torch.empty((M, N), dtype=torch.float32, device=X.device)
     wsp, wsb = _ws(ws)
     _check(getattr(load(), fn)(_dev(Wp, "Wp"), _dev(X, "X", numel=xbytes),
-                               _dev(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)), fn)
+                               _dev_or_host(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)),
+           fn)
     return out
 
 
@@ -228,8 +263,8 @@ def gemv_q4_0_q8_1_noalloc(Wp, Xq, N, K, out=None, stream=None):
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=Xq.device)
     _check(load().bqg_gemv_q4_0_q8_1_noalloc(_dev(Wp, "Wp"), _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
-                                             _dev(out, "Y", torch.float32, M * N * 4), M, N, K, _stream(stream)),
-           "bqg_gemv_q4_0_q8_1_noalloc")
+                                             _dev_or_host(out, "Y", torch.float32, M * N * 4), M, N, K,
+                                             _stream(stream)), "bqg_gemv_q4_0_q8_1_noalloc")
     return out
 
 

@@ -36,6 +36,7 @@ cudaError_t launch_rmsnorm_q8_1(const void *, int, const float *, float, void *,
 cudaError_t launch_quantize_weights(int, const float *, void *, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_repack(int, const void *, void *, int64_t, int64_t, cudaStream_t);
 cudaError_t launch_block_dots(const void *, const void *, int32_t *, int64_t, int64_t, int64_t, cudaStream_t);
+cudaError_t launch_copy_sm(void *, const void *, int64_t, int, cudaStream_t, bool);
 cudaError_t launch_splitk_reduce(const GemvParams &, int, int, int, cudaStream_t, bool);
 int gemm_bf16(int, const void *, const void *, float *, int, int64_t, int64_t, cudaStream_t, int);
 size_t gemm_workspace(int, int64_t, int64_t);
@@ -546,6 +547,33 @@ const char *bqg_version(void) { return "bqgemv 0.1 sm_103a"; }
 const char *bqg_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda); }
 
 int bqg_set_pdl(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
+int bqg_host_alias(const void *host, void **dev)
+{
+    if (!host || !dev) return BQG_ERR_INVALID_ARG;
+    DevInfo di;
+    if (int st = current_device(&di)) return st;
+    void *d = nullptr;
+    const cudaError_t e = cudaHostGetDevicePointer(&d, const_cast<void *>(host), 0);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();   // not page-locked and mapped: report it, leave no error pending
+        return cuda_status(e);
+    }
+    *dev = d;
+    return BQG_OK;
+}
+
+int bqg_copy_sm(void *dst, const void *src, size_t bytes, cudaStream_t stream)
+{
+    DevInfo dev;
+    if (bytes == 0) return current_device(&dev);   // nothing to copy: any pointers, no launch
+    if (!dst || !src) return BQG_ERR_INVALID_ARG;
+    if (!aligned16(dst) || !aligned16(src) || bytes % 16) return BQG_ERR_MISALIGNED;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst), b = reinterpret_cast<uintptr_t>(src);
+    if (a < b + bytes && b < a + bytes) return BQG_ERR_INVALID_ARG;   // overlapping ranges
+    if (int st = current_device(&dev)) return st;
+    return cuda_status(launch_copy_sm(dst, src, (int64_t)bytes, dev.sms, stream, g_pdl.load() != 0));
+}
 
 size_t bqg_repacked_size(int fmt, int64_t N, int64_t K)
 {

@@ -1,5 +1,6 @@
-// bqg_quant.cu -- block encoders, the load-time repack and the block-dot
-// debug export.
+// bqg_quant.cu -- block encoders, the load-time repack, the block-dot
+// debug export and the SM-driven copy (activations in, outputs out over the
+// coherent CPU-GPU link without a copy-engine transfer).
 //
 // Encoders (one warp per 32-element block, lane i = element i):
 //   q8_0 / q8_1 : d = fp16_rn(amax / 127), q = round_half_away(x / d) in
@@ -281,6 +282,29 @@ __global__ void __launch_bounds__(256) copy_u16_kernel(const uint16_t *__restric
         dst[i] = src[i];
 }
 
+// n pieces of 16 B from src to dst, copied by the SMs.  Either side may be
+// page-locked host memory mapped into the device's address space: each load
+// then crosses the CPU-GPU link, so every thread issues four before its
+// first store and the link's latency is paid about once per thread.  With
+// programmatic dependent launch the copy waits for the previous kernel
+// before it reads or writes anything.
+__global__ void __launch_bounds__(256) copy_sm_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                      int64_t n)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) v[u] = src[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; u++) dst[i + u * stride] = v[u];
+    }
+    for (; i < n; i += stride) dst[i] = src[i];
+}
+
 // The exact per-block integer dots of q4_0 x q8_1 (one activation row),
 // computed with the GEMV's own device routine (q4_0_q8_1_sumi).
 __global__ void __launch_bounds__(256) block_dots_kernel(const uint8_t *__restrict__ Wp, const uint8_t *__restrict__ Xq,
@@ -317,6 +341,24 @@ cudaError_t launch_quantize_q8_1(const void *x, int x_f32, void *xq, int M, int6
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel, x, x_f32, (uint8_t *)xq, nblocks, nb, K);
+}
+
+cudaError_t launch_copy_sm(void *dst, const void *src, int64_t bytes, int sms, cudaStream_t s, bool pdl)
+{
+    const int64_t n = bytes / 16;
+    // one 16-byte piece per thread up to four resident waves of CTAs, then grid-stride
+    const int64_t ctas = std::min<int64_t>((n + 255) / 256, (int64_t)sms * 4);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::max<int64_t>(ctas, 1));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, copy_sm_kernel, reinterpret_cast<const uint4 *>(src),
+                              reinterpret_cast<uint4 *>(dst), n);
 }
 
 cudaError_t launch_rmsnorm_q8_1(const void *x, int x_f32, const float *gamma, float eps, void *xq, int M, int64_t K,

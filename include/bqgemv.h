@@ -120,15 +120,19 @@ int bqg_quantize_q8_1(const void *x, int x_dtype, void *xq, int M, int64_t K,
 /* Fused RMSNorm + q8_1 quantization: the normalisation that precedes each
  * projection folded into the activation encoder, one launch instead of two
  * ("MI50 megakernel", hypothesis ledger: neighbouring steps fused into one
- * dispatch).  The pages name the fusion, not its arithmetic; per row m:
- *     s   = sum_k x[m,k]^2                 (fp64; exact for bf16 inputs)
- *     r   = fp32( 1 / sqrt(s / K + eps) )  (fp64 square root and division)
+ * dispatch).  The pages name the fusion, not its arithmetic; per row m
+ * the definition is
+ *     s   = sum_k x[m,k]^2                 (exact for bf16 inputs)
+ *     r   = fp32( 1 / sqrt(s / K + eps) )  (one rounding to fp32)
  *     y_k = fp32( fp32(x[m,k] * r) * gamma[k] )   (gamma NULL: no gain)
  * then y is encoded like bqg_quantize_q8_1.  x: M x K, x_dtype BQG_BF16 or
  * BQG_F32 (2- or 4-byte aligned); gamma: K fp32 or NULL (4-byte aligned);
  * eps >= 0 and finite; xq: M x K/32 blocks of 36 B (4-byte aligned);
- * 1 <= M <= 65535.  Bit-exact with that definition for bf16 inputs (for fp32
- * inputs the fp64 sum is exact up to its last bit). */
+ * 1 <= M <= 65535.  The kernel sums the squares as error-free fp32 pairs and
+ * refines rsqrtf by one Newton step; before its final rounding r is within
+ * about 2^-44 (relative) of the exact value, so r, and with it every byte,
+ * matches the definition evaluated in fp64 unless the exact value lies that
+ * close to an fp32 rounding boundary (about one row in 2^20). */
 int bqg_rmsnorm_quantize_q8_1(const void *x, int x_dtype, const float *gamma, float eps, void *xq, int M,
                               int64_t K, cudaStream_t stream);
 
@@ -137,7 +141,11 @@ int bqg_rmsnorm_quantize_q8_1(const void *x, int x_dtype, const float *gamma, fl
  * ws/ws_bytes: workspace for split-K; bqg_workspace_size(op, M, N, K) bytes
  * are required when that size is non-zero (BQG_ERR_WORKSPACE otherwise); it
  * needs no initialisation and must not be shared by calls that overlap.
- * fp32 accumulation; bqg_gemv_q8_0/q4_0 dequantize (q*d, (q-8)*d) exactly. */
+ * fp32 accumulation; bqg_gemv_q8_0/q4_0 dequantize (q*d, (q-8)*d) exactly.
+ * Y may also be page-locked host memory given by its bqg_host_alias address
+ * (the outputs are written there with plain stores over the CPU-GPU link);
+ * this holds for the four bqg_gemv_* entries of a single matrix and
+ * bqg_gemv_q4_0_q8_1_noalloc.  X and Wp must be device memory. */
 int bqg_gemv_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
                   void *ws, size_t ws_bytes, cudaStream_t stream);
 int bqg_gemv_q8_0(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
@@ -271,6 +279,29 @@ size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K);
  * wait sets when it gives up (0 = none).  Synchronizes `stream` first.
  * Returns BQG_OK or BQG_ERR_CUDA; *out receives the word. */
 int bqg_last_device_error(cudaStream_t stream, int *out);
+
+/* ---- host memory on the coherent CPU-GPU link ------------------------- */
+
+/* Device-side address of page-locked host memory (cudaHostAlloc,
+ * cudaMallocHost, or cudaHostRegister with mapping); under unified
+ * addressing it equals `host`.  Kernels that read or write it cross the
+ * CPU-GPU link (NVLink-C2C on a Grace node) with no copy-engine transfer.
+ * *dev receives the address.  BQG_ERR_INVALID_ARG for null arguments;
+ * BQG_ERR_CUDA when the memory is not page-locked and mapped (nothing is
+ * left pending on the CUDA runtime). */
+int bqg_host_alias(const void *host, void **dev);
+
+/* Copy `bytes` from src to dst with a kernel (the SMs) instead of a copy
+ * engine: for moving an activation row in from, or a result out to, memory
+ * named by bqg_host_alias, where a copy-engine transfer of a few KB costs
+ * more in latency than the bytes.  Either pointer may be device memory or a
+ * host alias.  Ordered on `stream` like any launch; with programmatic
+ * dependent launch on (bqg_set_pdl) it waits for the previous kernel before
+ * it reads or writes anything.  Both pointers 16-byte aligned and bytes a
+ * multiple of 16 (BQG_ERR_MISALIGNED); the ranges must not overlap
+ * (BQG_ERR_INVALID_ARG).  bytes = 0 launches nothing and accepts any
+ * pointers (null included). */
+int bqg_copy_sm(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 
 /* Programmatic dependent launch for the GEMV kernels (default off).
  * When on, a GEMV may start and begin streaming its weights while the

@@ -94,6 +94,14 @@ FAKE = 0x10000  # never dereferenced: every call below fails validation first
     (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 0, FAKE + 8, *[FAKE] * 9, 1, 64, 64, 128, 64, FAKE, 1 << 20,
                                             None), 3),
     (lambda L: L.bqg_decode_layer_q4_0_q8_1(FAKE, FAKE, 0, *[FAKE] * 10, 1, 64, 64, 128, 64, FAKE, 64, None), 7),
+    # SM copy and host alias: (dst, src, bytes, stream), (host, &dev)
+    (lambda L: L.bqg_copy_sm(None, FAKE, 16, None), 1),
+    (lambda L: L.bqg_copy_sm(FAKE, FAKE + 0x1008, 16, None), 3),       # src not 16-byte aligned
+    (lambda L: L.bqg_copy_sm(FAKE, FAKE + 0x1000, 24, None), 3),       # bytes % 16
+    (lambda L: L.bqg_copy_sm(FAKE + 16, FAKE, 64, None), 1),           # overlapping ranges
+    (lambda L: L.bqg_copy_sm(FAKE, FAKE + 48, 64, None), 1),
+    (lambda L: L.bqg_host_alias(None, FAKE), 1),
+    (lambda L: L.bqg_host_alias(FAKE, None), 1),
 ])
 def test_host_validation_rejects_before_launch(L, call, status):
     assert call(L) == status
@@ -109,6 +117,10 @@ def test_no_device_is_an_error_not_a_fallback(L):
     assert L.bqg_workspace_size(0, 1, 8, 64) == 0
     out = ctypes.c_int(0)
     assert L.bqg_last_device_error(None, None) == 1
+    assert L.bqg_copy_sm(FAKE, FAKE + 0x1000, 16, None) in (4, 5)
+    dev = ctypes.c_void_p(0)
+    assert L.bqg_host_alias(FAKE, ctypes.addressof(dev)) in (4, 5)
+    assert L.bqg_copy_sm(FAKE, FAKE + 0x1000, 0, None) in (4, 5)    # even an empty copy checks the device
 
 
 def test_pdl_switch_roundtrip(L):
