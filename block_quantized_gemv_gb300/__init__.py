@@ -3,9 +3,12 @@
 A thin ctypes layer over the C ABI in include/bqgemv.h: every function here
 has the name of its C entry point without the ``bqg_`` prefix, checks that
 the torch tensors it is given match the C contract, and passes raw device
-pointers plus the current CUDA stream.  All arithmetic runs in the library's
-CUDA kernels; PyTorch only provides device memory and streams.  There is no
-fallback: if the shared library is missing, every call raises.
+pointers plus the current CUDA stream.  Where the C contract allows host
+memory (the output of a single-matrix GEMV, either side of copy_sm), a pinned
+CPU tensor is passed as its device-side alias (bqg_host_alias).  All
+arithmetic runs in the library's CUDA kernels; PyTorch only provides memory
+and streams.  There is no fallback: if the shared library is missing, every
+call raises.
 """
 from __future__ import annotations
 
