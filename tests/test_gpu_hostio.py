@@ -6,7 +6,7 @@ outputs written straight into page-locked host memory.
     tails, and writes nothing past the end;
   * a GEMV given a pinned host Y writes the same bits as the same call with a
     device Y (same kernel, same order), on the single-pass and the split-K
-    paths, and those bits meet the north-star bound against the oracle;
+    paths, and those bits are within |dy| <= 1e-3 * sum|w x| + 1e-6 of the oracle;
   * a chain of steps (copy in, GEMV out) enqueued back to back with
     programmatic dependent launch on keeps stream order: every step sees its
     own activation and leaves its own output.
