@@ -89,15 +89,25 @@ def whole_job_gbs(bytes_per_call, calls_per_rank, world, seconds):
     return bytes_per_call * calls_per_rank * world / seconds / 1e9
 
 
-def divisor_repeats(K, cap=10):
-    for r in range(min(cap, K), 0, -1):
-        if K % r == 0:
-            return r
-    return 1
+# The instrument of "The Shape That Actually Matters", "The instrument came
+# first": 200 timed launches per repeat, 10 repeats, and no number unless the
+# spread of the repeat means is below 5 % of their mean.
+REPEATS = 10
+MIN_LAUNCHES_PER_REPEAT = 200
+MAX_SPREAD = 0.05
+ATTEMPTS = 3            # the measurement and at most two re-measurements
+
+
+def protocol_launches(steps):
+    """(repeats, launches per repeat) for a run asked for `steps` timed
+    calls: always 10 repeats of at least 200 launches; more launches per
+    repeat when `steps` asks for more."""
+    return REPEATS, max(MIN_LAUNCHES_PER_REPEAT, -(-int(steps) // REPEATS))
 
 
 class NvmlSampler:
-    """Samples SM clock and clock-event reasons through NVML (read-only)."""
+    """Samples SM clock, temperature, power and clock-event reasons through
+    NVML (read-only calls only)."""
 
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
@@ -127,15 +137,20 @@ class NvmlSampler:
 
     def _loop(self):
         clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        temp, mw = ctypes.c_uint(0), ctypes.c_uint(0)
         while not self._stop.is_set():
             if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0 and \
                     self.reason_fn(self.h, ctypes.byref(rs)) == 0:
-                self.samples.append((clk.value, rs.value))
-            time.sleep(0.002)
+                t = temp.value if self.nv.nvmlDeviceGetTemperature(self.h, 0, ctypes.byref(temp)) == 0 else None
+                w = mw.value / 1000.0 if self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw)) == 0 else None
+                self.samples.append((clk.value, rs.value, t, w))
+            time.sleep(0.001)
 
     def start(self):
+        """Start a fresh record (samples of an earlier region are dropped)."""
         if not self.ok:
             return
+        self.samples = []
         self._stop = threading.Event()
         self._t = threading.Thread(target=self._loop, daemon=True)
         self._t.start()
@@ -150,18 +165,37 @@ class NvmlSampler:
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
                     "source": "nvml" if self.ok else "unavailable"}
-        mhz = [c for c, _ in self.samples]
+        mhz = [c for c, _, _, _ in self.samples]
+        temps = [t for _, _, t, _ in self.samples if t is not None]
+        watts = [w for _, _, _, w in self.samples if w is not None]
         mask = 0
-        for _, r in self.samples:
+        for _, r, _, _ in self.samples:
             mask |= r
         reasons = [n for b, n in self.REASONS.items() if mask & b and n != "gpu_idle"]
-        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
-                "samples": len(self.samples), "source": "nvml"}
+        return {"sm_mhz": statistics.median(mhz), "sm_mhz_min": min(mhz), "sm_max_mhz": self.max_mhz,
+                "temp_c_max": max(temps) if temps else None,
+                "power_w_median": round(statistics.median(watts), 1) if watts else None,
+                "power_w_max": round(max(watts), 1) if watts else None,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml"}
 
 
 # ---------------------------------------------------------------------------
 # workloads ("arms")
 # ---------------------------------------------------------------------------
+_W_CACHE = {}
+
+
+def cached_weights(N, K, seed):
+    """synth.weights_f32(N, K, seed), remembered for the next arm of the same
+    shape (the sweep's formats share their fp32 weights); one entry."""
+    from block_quantized_gemv_gb300 import synth
+    key = (N, K, seed)
+    if key not in _W_CACHE:
+        _W_CACHE.clear()
+        _W_CACHE[key] = synth.weights_f32(N, K, seed)
+    return _W_CACHE[key]
+
+
 class Arm:
     """One call = one pass over one weight set; `sets` rotate."""
     name = ""
@@ -189,7 +223,7 @@ class GemvArm(Arm):
         self.name = f"{names[fmt]} x {xs} GEMV M={M} K={K} N={N}"
         self.kernel_key = f"gemv_{names[fmt]}_{xs}_M{M}_K{K}_N{N}"
         # weights: fp32 N(0, 0.02) -> (GPU encoder) -> canonical -> (GPU repack)
-        Wf = torch.from_numpy(synth.weights_f32(N, K, seed)).cuda()
+        Wf = torch.from_numpy(cached_weights(N, K, seed)).cuda()
         if fmt == bqg.BF16:
             canon = Wf.to(torch.bfloat16).view(torch.uint8).reshape(-1)
         else:
@@ -255,7 +289,7 @@ class VendorGemvArm(Arm):
         self.M, self.N, self.K = M, N, K
         self.name = f"vendor arm: torch.matmul (cuBLAS) bf16 GEMV M={M} K={K} N={N}"
         self.kernel_key = ""
-        W = torch.from_numpy(synth.weights_f32(N, K, seed)).cuda().to(torch.bfloat16)
+        W = torch.from_numpy(cached_weights(N, K, seed)).cuda().to(torch.bfloat16)
         x = torch.from_numpy(synth.activations_f32(M, K, seed + 1)).cuda().to(torch.bfloat16)
         self.bytes_per_call = N * K * 2 + M * K * 2 + M * N * 2
         self.R = self.rotation(self.bytes_per_call)
@@ -283,7 +317,7 @@ class GemmArm(Arm):
         self.fn = bqg.gemm_q8_0_bf16 if fmt == bqg.Q8_0 else bqg.gemm_q4_0_bf16
         self.name = f"{fname} x bf16 prefill GEMM M={M} K={K} N={N}"
         self.kernel_key = f"gemm_{fname}_bf16_M{M}_K{K}_N{N}"
-        Wf = torch.from_numpy(synth.weights_f32(N, K, seed)).cuda()
+        Wf = torch.from_numpy(cached_weights(N, K, seed)).cuda()
         Wp = bqg.repack_weights(fmt, bqg.quantize_weights(fmt, Wf), N, K)
         del Wf
         X = torch.from_numpy(synth.activations_f32(M, K, seed + 1)).cuda().to(torch.bfloat16)
@@ -331,7 +365,7 @@ class DecodeLayerArm(Arm):
         self.K, self.Nq, self.Nff = K, Nq, Nff
 
         def mk(N, KK, sd):
-            Wf = torch.from_numpy(synth.weights_f32(N, KK, sd)).cuda()
+            Wf = torch.from_numpy(cached_weights(N, KK, sd)).cuda()
             return bqg.repack_weights(bqg.Q4_0, bqg.quantize_weights(bqg.Q4_0, Wf), N, KK)
 
         base = {"Wq": mk(Nq, K, seed), "Wk": mk(Nq, K, seed + 1), "Wv": mk(Nq, K, seed + 2),
@@ -390,9 +424,13 @@ class DecodeLayerArm(Arm):
 # timing
 # ---------------------------------------------------------------------------
 def time_arm(arm, steps, warmup, use_graph=True, min_warm_s=1.0, sampler=None, dist=None):
+    """One measurement of `arm` under the protocol: 10 repeats of L >= 200
+    launches (one CUDA graph of L calls rotating through the buffer sets, so
+    every call streams its inputs from HBM), warm-up of at least `warmup`
+    calls and `min_warm_s` seconds on the same rotation, CUDA events on the
+    launching stream around each repeat, NVML sampled over the timed region."""
     import torch
-    repeats = divisor_repeats(steps)
-    L = steps // repeats
+    repeats, L = protocol_launches(steps)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -443,11 +481,31 @@ def time_arm(arm, steps, warmup, use_graph=True, min_warm_s=1.0, sampler=None, d
     total = max_over_ranks(sum(times), dist)
     mean = statistics.mean(times)
     spread = (max(times) - min(times)) / mean if mean > 0 else 0.0
+    spread = max_over_ranks(spread, dist)
+    del graph
     return {"seconds": total, "per_repeat_s": times, "repeats": repeats, "launches_per_repeat": L,
-            "spread": spread, "spread_ok": spread < 0.05, "graph": graph is not None}
+            "timed_calls": repeats * L, "spread": spread, "spread_ok": spread < MAX_SPREAD,
+            "graph": use_graph, "clocks": sampler.summary() if sampler else None}
+
+
+def measure(arm, steps, warmup, **kw):
+    """time_arm under the rejection rule: re-measured while the repeat spread
+    is >= 5 %, at most ATTEMPTS times in all; the last attempt is returned
+    with `rejected` set when its spread still fails."""
+    spreads = []
+    for _ in range(ATTEMPTS):
+        t = time_arm(arm, steps, warmup, **kw)
+        spreads.append(round(t["spread"], 4))
+        if t["spread_ok"]:
+            break
+    t["attempt_spreads"] = spreads
+    t["rejected"] = not t["spread_ok"]
+    return t
 
 
 def time_e2e(arm, steps, step_fn=None):
+    """Device time of `steps` end-to-end steps enqueued back to back (CUDA
+    events on the launching stream)."""
     import torch
     step = step_fn or arm.call_e2e
     stream = torch.cuda.Stream()
@@ -464,21 +522,48 @@ def time_e2e(arm, steps, step_fn=None):
     return a.elapsed_time(b) / 1e3
 
 
+def time_e2e_host(arm, steps, step_fn=None):
+    """Host-clock time per step of a decode loop: every step is the binding
+    call(s) from pinned x to pinned y followed by a stream synchronize, timed
+    with time.perf_counter (the latency an autoregressive host loop sees,
+    host launch cost included).  Returns the median and mean seconds per step."""
+    import torch
+    step = step_fn or arm.call_e2e
+    stream = torch.cuda.Stream()
+    per = []
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            step(i)
+            stream.synchronize()
+        for i in range(steps):
+            t0 = time.perf_counter()
+            step(i)
+            stream.synchronize()
+            per.append(time.perf_counter() - t0)
+    return statistics.median(per), statistics.mean(per)
+
+
 def gb_s(bytes_, seconds):
     return bytes_ / seconds / 1e9
 
 
 def arm_record(arm, t, peaks):
+    """The arm's record.  A rejected measurement (repeat spread still >= 5 %
+    after the re-measurements) carries no rate: only its spreads."""
     calls = t["repeats"] * t["launches_per_repeat"]
-    us = t["seconds"] / calls * 1e6
-    gbs = gb_s(arm.bytes_per_call * calls, t["seconds"])
-    rec = {"workload": arm.name, "us_per_call": round(us, 3), "GB_per_s": round(gbs, 1),
-           "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_call": arm.bytes_per_call,
+    rec = {"workload": arm.name, "bytes_per_call": arm.bytes_per_call,
            "rotating_sets": arm.R, "working_set_bytes": arm.R * arm.bytes_per_call,
+           "repeats": t["repeats"], "launches_per_repeat": t["launches_per_repeat"], "timed_calls": calls,
            "spread": round(t["spread"], 4), "spread_ok": t["spread_ok"],
-           "launches": calls * arm.launches_per_call}
+           "attempt_spreads": t.get("attempt_spreads"), "rejected": t.get("rejected", not t["spread_ok"]),
+           "launches": calls * arm.launches_per_call, "clocks": t.get("clocks")}
     if getattr(arm, "vendor", False):
         rec["vendor"] = "library GEMV for context (cuBLAS through torch.matmul), not this repository's kernels"
+    if rec["rejected"]:
+        return rec
+    us = t["seconds"] / calls * 1e6
+    gbs = gb_s(arm.bytes_per_call * calls, t["seconds"])
+    rec.update({"us_per_call": round(us, 3), "GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4)})
     if getattr(arm, "flops", None):
         tf = arm.flops * calls / t["seconds"] / 1e12
         rec.update({"bound": "tensor", "TFLOP_per_s": round(tf, 1),
@@ -491,14 +576,19 @@ def arm_record(arm, t, peaks):
 # ---------------------------------------------------------------------------
 # the CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
-def oracle_gemv_sample(rows_per_step, steps, budget_s=None):
-    """Time the fp64 oracle on the headline workload, `rows_per_step` rows per step."""
-    import oracle
+def _oracle_headline_inputs():
     from block_quantized_gemv_gb300 import synth
-    ora = oracle.default()
-    Wf = synth.weights_f32(N_HEAD, K_HEAD, 1)
-    W = synth.bf16_bits(Wf)
+    W = synth.bf16_bits(synth.weights_f32(N_HEAD, K_HEAD, 1))
     X = synth.bf16_bits(synth.activations_f32(1, K_HEAD, 2))
+    return W, X
+
+
+def oracle_gemv_sample(rows_per_step, steps, budget_s=None):
+    """Time the fp64 oracle on the headline workload, `rows_per_step` rows per
+    step (a different slice every step), OpenMP over rows on every core."""
+    import oracle
+    ora = oracle.default()
+    W, X = _oracle_headline_inputs()
     threads = max(1, os.cpu_count() or 1)
     rng = np.random.default_rng(0)
     starts = rng.integers(0, N_HEAD - rows_per_step + 1, size=max(1, steps))
@@ -518,16 +608,58 @@ def oracle_gemv_sample(rows_per_step, steps, budget_s=None):
             "threads_used": threads, "seconds": dt, "steps": done, "rows_per_step": rows_per_step}
 
 
+def oracle_baseline(runs=5, run_s=1.0):
+    """The oracle as it stands, timed on the host's cores in both of its
+    modes: one thread, and OpenMP over output rows on every core (each row's
+    fp64 sum keeps its order, so both give the same results).  A run is as
+    many whole headline GEMVs (12288 x 4096 bf16) as fit in about `run_s`
+    seconds (at least one); each mode reports the median of `runs` runs."""
+    import oracle
+    ora = oracle.default()
+    W, X = _oracle_headline_inputs()
+    bytes_per_call = N_HEAD * K_HEAD * 2 + K_HEAD * 2 + N_HEAD * 4
+    cores = os.cpu_count() or 1
+    modes = {}
+    for name, threads in (("single_thread", 1), ("openmp", cores)):
+        rates, calls_per_run = [], []
+        for _ in range(runs):
+            t0 = time.perf_counter()
+            n = 0
+            while n == 0 or time.perf_counter() - t0 < run_s:
+                ora.gemv(oracle.BF16, W, oracle.BF16, X, 1, N_HEAD, K_HEAD, nthreads=threads)
+                n += 1
+            dt = time.perf_counter() - t0
+            rates.append(gb_s(bytes_per_call * n, dt))
+            calls_per_run.append(n)
+        med = statistics.median(rates)
+        modes[name] = {"value": round(med, 4), "unit": "GB/s", "threads": threads,
+                       "us_per_call": round(bytes_per_call / (med * 1e9) * 1e6, 1),
+                       "runs": [round(r, 4) for r in rates], "calls_per_run": calls_per_run}
+    return {"value": modes["openmp"]["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"whole headline GEMVs (12288 x 4096 bf16 weights) of the fp64 C oracle, runs of about "
+                      f"{run_s:g} s, median of {runs} runs per mode; value = the OpenMP mode on all "
+                      f"{cores} host cores (os.cpu_count())",
+            "modes": modes}
+
+
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
+def headline_config():
+    """The workload both arms (this library and the oracle) report."""
+    return {"workload": f"bf16 GEMV M=1 K={K_HEAD} N={N_HEAD}", "M": 1, "K": K_HEAD, "N": N_HEAD,
+            "weights": "bf16 N(0,0.02), activation bf16 N(0,1), fp32 output"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--suite", choices=["headline", "full"], default="headline")
+    ap.add_argument("--suite", choices=["headline", "full"], default="full",
+                    help="full (default): every configuration; headline: the M=1 K=4096 N=12288 arms, "
+                         "the prefill GEMM and the vendor arm")
     ap.add_argument("--pdl", type=int, default=1)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -542,23 +674,21 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     headline_metric = "cold-cache HBM GB/s (% of peak) and µs/call, GEMV M=1 K=4096 N=12288"
-    workload = f"bf16 GEMV M=1 K={K_HEAD} N={N_HEAD}"
 
     if args.impl == "reference":
         if rank != 0:
             return 0
-        rows = max(64, N_HEAD // 16)
-        r = oracle_gemv_sample(rows, args.steps + args.warmup)
+        r = oracle_gemv_sample(N_HEAD, args.steps + args.warmup)
         out = {"impl": "reference", "metric": headline_metric, "value": r["value"], "unit": "GB/s",
                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                "ms_per_step": round(r["seconds"] / max(1, r["steps"]) * 1e3, 4),
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-               "data": "synthetic",
-               "config": {"workload": workload, "reference": "CPU oracle (fp64, plain C), the only "
-                          "implementation the pages provide a definition for; no code was published"},
+               "data": "synthetic", "config": headline_config(),
+               "reference": "the CPU oracle (fp64, plain C, OpenMP over rows), the only implementation of the "
+                            "pages' definition: the pages publish no code",
                "cpu_baseline": {"kind": "oracle", "value": r["value"], "unit": "GB/s", "cores": r["threads_used"],
-                                "sample": f"{rows} consecutive rows of the 12288 x 4096 bf16 matrix per step "
-                                          f"(every step a different sample), {r['steps']} steps"},
+                                "sample": f"{r['steps']} whole GEMVs (12288 x 4096 bf16 weights), one per step, "
+                                          f"warm-up included in the count ({args.warmup} + {args.steps})"},
                "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(out))
         return 0
@@ -605,87 +735,99 @@ def main():
         return 0
 
     head = GemvArm(bqg.BF16, bqg.BF16, 1, N_HEAD, K_HEAD)
-    t = time_arm(head, args.steps, args.warmup, use_graph=not args.no_graph, min_warm_s=args.min_warm_s,
-                 sampler=sampler, dist=dist)
-    if not t["spread_ok"]:       # protocol: reject and measure once more
-        t2 = time_arm(head, args.steps, args.warmup, use_graph=not args.no_graph, min_warm_s=args.min_warm_s,
-                      sampler=sampler, dist=dist)
-        t2["first_attempt_spread"] = t["spread"]
-        t = t2
+    kw = dict(use_graph=not args.no_graph, sampler=sampler, dist=dist)
+    t = measure(head, args.steps, args.warmup, min_warm_s=args.min_warm_s, **kw)
     rec = arm_record(head, t, peaks)
-    calls = args.steps
-    value = whole_job_gbs(head.bytes_per_call, calls, world, t["seconds"])
-    clocks = sampler.summary()
+    calls = t["timed_calls"]
+    rejected = t["rejected"]
+    value = None if rejected else whole_job_gbs(head.bytes_per_call, calls, world, t["seconds"])
 
-    e2e_s = time_e2e(head, args.steps)
-    ce_s = time_e2e(head, args.steps, head.call_e2e_copy_engine)
-    e2e = {"value": round(gb_s(head.bytes_per_call * args.steps, e2e_s), 1), "unit": "GB/s",
+    e2e_steps = max(args.steps, MIN_LAUNCHES_PER_REPEAT)
+    e2e_s = time_e2e(head, e2e_steps)
+    ce_s = time_e2e(head, e2e_steps, head.call_e2e_copy_engine)
+    host_med, host_mean = time_e2e_host(head, e2e_steps)
+    host_ce_med, _ = time_e2e_host(head, e2e_steps, head.call_e2e_copy_engine)
+    e2e = {"value": round(gb_s(head.bytes_per_call * e2e_steps, e2e_s), 1), "unit": "GB/s",
            "h2d_bytes_per_step": head.x_bytes, "d2h_bytes_per_step": head.y_bytes,
-           "us_per_step": round(e2e_s / args.steps * 1e6, 3),
+           "steps": e2e_steps, "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
+           "timing": "CUDA events around the steps enqueued back to back on one stream",
+           "host_us_per_step": round(host_med * 1e6, 3), "host_us_per_step_mean": round(host_mean * 1e6, 3),
+           "host_value": round(gb_s(head.bytes_per_call, host_med), 1),
+           "host_timing": "time.perf_counter around each step (binding calls, then stream.synchronize): "
+                          "the per-token latency a host decode loop sees, median over the steps",
            "path": "through the Python binding, every step: x from pinned host memory into device memory by "
                    "bqg_copy_sm (SM loads over the CPU-GPU link), bqg_gemv_bf16 writing y straight into pinned "
                    "host memory (bqg_host_alias); the host reads y there after the final synchronize",
-           "copy_engine": {"value": round(gb_s(head.bytes_per_call * args.steps, ce_s), 1), "unit": "GB/s",
-                           "us_per_step": round(ce_s / args.steps * 1e6, 3),
+           "copy_engine": {"value": round(gb_s(head.bytes_per_call * e2e_steps, ce_s), 1), "unit": "GB/s",
+                           "us_per_step": round(ce_s / e2e_steps * 1e6, 3),
+                           "host_us_per_step": round(host_ce_med * 1e6, 3),
                            "path": "the same step with torch copies (copy-engine transfers) of x in and y out"}}
 
     arms = [rec]
-    other = [GemvArm(bqg.Q8_0, bqg.BF16, 1, N_HEAD, K_HEAD), GemvArm(bqg.Q4_0, bqg.Q8_1, 1, N_HEAD, K_HEAD),
-             GemmArm(), VendorGemvArm(1, N_HEAD, K_HEAD)]
+    specs = [lambda: GemvArm(bqg.Q8_0, bqg.BF16, 1, N_HEAD, K_HEAD),
+             lambda: GemvArm(bqg.Q4_0, bqg.Q8_1, 1, N_HEAD, K_HEAD),
+             lambda: GemmArm(), lambda: VendorGemvArm(1, N_HEAD, K_HEAD)]
     if args.suite == "full":
-        other += [GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096), DecodeLayerArm(), DecodeLayerArm(fused_norm=True),
-                  DecodeLayerArm(persistent=True),
-                  GemmArm(fmt=bqg.Q8_0)]
+        specs += [lambda: GemmArm(fmt=bqg.Q8_0), lambda: GemvArm(bqg.Q8_0, bqg.BF16, 1, 4096, 4096),
+                  lambda: DecodeLayerArm(), lambda: DecodeLayerArm(fused_norm=True),
+                  lambda: DecodeLayerArm(persistent=True)]
         for M in (1, 2, 4, 8):
             for f in (bqg.BF16, bqg.Q8_0, bqg.Q4_0):
-                other.append(GemvArm(f, bqg.BF16, M, 14336, 4096))
-            other.append(GemvArm(bqg.Q4_0, bqg.Q8_1, M, 14336, 4096))
-    for a in other:
-        ta = time_arm(a, args.steps, max(3, args.warmup // 4), use_graph=not args.no_graph,
-                      min_warm_s=min(0.3, args.min_warm_s), dist=dist)
-        arms.append(arm_record(a, ta, peaks))
+                specs.append(lambda M=M, f=f: GemvArm(f, bqg.BF16, M, 14336, 4096))
+            specs.append(lambda M=M: GemvArm(bqg.Q4_0, bqg.Q8_1, M, 14336, 4096))
+    launches_all = calls * head.launches_per_call
+    for mk in specs:
+        a = mk()
+        ta = measure(a, args.steps, max(3, args.warmup // 4), min_warm_s=min(0.3, args.min_warm_s), **kw)
+        r = arm_record(a, ta, peaks)
+        arms.append(r)
+        launches_all += r["launches"]
         del a
         torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = oracle_gemv_sample(N_HEAD, 1000, budget_s=10.0)
-        cpu = {"value": r["value"], "unit": "GB/s", "cores": r["threads_used"], "kind": "oracle",
-               "sample": f"{r['steps']} full GEMV calls (12288 rows x 4096, bf16 weights) of the fp64 C oracle, "
-                         f"OpenMP over rows, ~10 s budget"}
+        cpu = oracle_baseline()
 
-    achieved = rec["GB_per_s"]
     traffic = profiled_traffic(head.kernel_key)
+    knobs = {k: v for k, v in sorted(os.environ.items()) if k.startswith("BQG_")}
     out = {
         "metric": headline_metric,
-        "value": round(value, 1),
+        "value": None if value is None else round(value, 1),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(t["seconds"] / calls * 1e3, 6),
+        "ms_per_step": None if rejected else round(t["seconds"] / calls * 1e3, 6),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": workload, "M": 1, "K": K_HEAD, "N": N_HEAD,
-                   "weights": "bf16 N(0,0.02), activation bf16 N(0,1), fp32 output",
-                   "rotating_weight_sets": head.R, "working_set_bytes": head.R * head.bytes_per_call,
-                   "l2_bytes": props.L2_cache_size,
-                   "cold_cache": "inputs larger than L2: rotating buffer sets, >= 1 GiB working set",
-                   "timing": "CUDA graph of the timed launches, CUDA events on the launching stream",
-                   "pdl": bool(args.pdl), "repeats": t["repeats"], "launches_per_repeat": t["launches_per_repeat"],
-                   "spread": round(t["spread"], 4), "spread_ok": t["spread_ok"],
-                   "us_per_call": rec["us_per_call"], "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
-                     "algorithmic_bytes_per_launch": head.bytes_per_call},
+        "rejected": rejected,
+        "timed_launches": calls,
+        "config": headline_config(),
+        "protocol": {"step": "one GEMV call (one pass of the path over one activation row)",
+                     "repeats": t["repeats"], "launches_per_repeat": t["launches_per_repeat"],
+                     "timed_calls": calls, "spread": round(t["spread"], 4), "spread_ok": t["spread_ok"],
+                     "attempt_spreads": t["attempt_spreads"], "max_spread": MAX_SPREAD,
+                     "rotating_weight_sets": head.R, "working_set_bytes": head.R * head.bytes_per_call,
+                     "l2_bytes": props.L2_cache_size,
+                     "cold_cache": "inputs larger than L2: rotating buffer sets, >= 1 GiB working set",
+                     "timing": "CUDA graph of the launches of a repeat, CUDA events on the launching stream",
+                     "us_per_call": rec.get("us_per_call"),
+                     "parallelism": "replicas" if world > 1 else "single GPU"},
+        "library": {"pdl": bool(args.pdl), "env_knobs": knobs, "version": bqg.version()},
+        "roofline": None if rejected else {
+            "bound": "hbm", "achieved": rec["GB_per_s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(rec["GB_per_s"] / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+            "algorithmic_bytes_per_launch": head.bytes_per_call},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": calls,
-        "clocks": clocks,
+        "gpu_launches": calls * head.launches_per_call,
+        "gpu_launches_all_arms": launches_all,
+        "clocks": t["clocks"],
         "arms": arms,
     }
     if rank == 0:

@@ -8,7 +8,8 @@ memory (the output of a single-matrix GEMV, either side of copy_sm), a pinned
 CPU tensor is passed as its device-side alias (bqg_host_alias).  All
 arithmetic runs in the library's CUDA kernels; PyTorch only provides memory
 and streams.  There is no fallback: if the shared library is missing, every
-call raises.
+call raises.  Every CUDA tensor must be on the current device (ValueError
+otherwise, before anything is launched).
 """
 from __future__ import annotations
 
@@ -47,6 +48,7 @@ EXPORTS = {
     "bqg_gemm_q4_0_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_gemm_q8_0_bf16": (["p", "p", "p", "i", "i64", "i64", "p", "size", "p"], "i"),
     "bqg_debug_q4_0_q8_1_block_dots": (["p", "p", "p", "i64", "i64", "p"], "i"),
+    "bqg_debug_q4_0_q8_1_block_dots_kslice": (["p", "p", "p", "i64", "i64", "p"], "i"),
     "bqg_workspace_size": (["i", "i", "i64", "i64"], "size"),
     "bqg_last_device_error": (["p", "p"], "i"),
     "bqg_set_pdl": (["i"], "i"),
@@ -119,9 +121,23 @@ def _stream(stream=None) -> int:
     return torch.cuda.current_stream().cuda_stream
 
 
+def _current_device() -> int:
+    return _cur_device() if _cur_device is not None else torch.cuda.current_device()
+
+
+def check_device(index: int, current: int, name: str) -> None:
+    """A CUDA tensor must live on the current device: the library launches
+    on the current device and would otherwise dereference another GPU's
+    memory."""
+    if index != current:
+        raise ValueError(f"{name} is on cuda:{index} but the current device is cuda:{current}; "
+                         f"call under torch.cuda.device({index})")
+
+
 def _dev(t: torch.Tensor, name: str, dtype=None, numel=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    check_device(t.device.index, _current_device(), name)
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -370,13 +386,23 @@ def gemm_q8_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
     return out
 
 
-def debug_q4_0_q8_1_block_dots(Wp, Xq, N, K, out=None, stream=None):
+def _block_dots(fn, Wp, Xq, N, K, out, stream):
     if out is None:
         out = torch.empty((N, K // QK), dtype=torch.int32, device=Xq.device)
-    _check(load().bqg_debug_q4_0_q8_1_block_dots(_dev(Wp, "Wp"), _dev(Xq, "Xq", numel=row_bytes(Q8_1, K)),
-                                                 _dev(out, "dots", torch.int32, N * (K // QK) * 4), N, K,
-                                                 _stream(stream)), "bqg_debug_q4_0_q8_1_block_dots")
+    _check(getattr(load(), fn)(_dev(Wp, "Wp"), _dev(Xq, "Xq", numel=row_bytes(Q8_1, K)),
+                               _dev(out, "dots", torch.int32, N * (K // QK) * 4), N, K, _stream(stream)), fn)
     return out
+
+
+def debug_q4_0_q8_1_block_dots(Wp, Xq, N, K, out=None, stream=None):
+    """The integer block dots as gemv_q4_0_q8_1 computes them at M = 1 (its
+    own kernel and plan), N x K/32 int32."""
+    return _block_dots("bqg_debug_q4_0_q8_1_block_dots", Wp, Xq, N, K, out, stream)
+
+
+def debug_q4_0_q8_1_block_dots_kslice(Wp, Xq, N, K, out=None, stream=None):
+    """The same dots from the K-slice kernel's routine."""
+    return _block_dots("bqg_debug_q4_0_q8_1_block_dots_kslice", Wp, Xq, N, K, out, stream)
 
 
 # --- utilities -----------------------------------------------------------------

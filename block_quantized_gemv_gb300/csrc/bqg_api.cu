@@ -24,6 +24,7 @@ cudaError_t gemv_lpr_run_bf16(const GemvParams &, int, dim3, int, size_t, cudaSt
 cudaError_t gemv_lpr_run_q8_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_lpr_run_q4_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_lpr_dots_run_q4_0_q8_1(const GemvParams &, dim3, int, size_t, cudaStream_t, int *);
 int gemv_x_stage_bytes_bf16(int, int, int);
 int gemv_x_stage_bytes_q8_0(int, int, int);
 int gemv_x_stage_bytes_q4_0(int, int, int);
@@ -419,6 +420,34 @@ size_t swiglu_q8_1_staging(int M, int64_t N)
     return ((size_t)M * N * 4 + 15) / 16 * 16 + (size_t)M * (N / 32) * 4;
 }
 
+// The plan's geometry in the kernel parameters.
+void apply_plan(GemvParams &p, const GemvPlan &g, int64_t K)
+{
+    p.K = (int)K;
+    p.nb = (int)(K / QK);
+    p.nc = g.nc;
+    p.TPR = g.TPR;
+    p.RG = g.RG;
+    p.chunks_per_split = g.cps;
+    p.nstages = g.NS;
+    p.stage_rows = g.S;
+    p.row_stride = g.stride;
+    p.win_stages = g.win_stages;
+    p.part_off = g.part_off;
+    p.bar_off = g.bar_off;
+    p.ctas = g.ctas;
+    p.L = g.L;
+    p.wg = g.wg;
+    p.ng = g.ng;
+    p.x_off = g.x_off;
+    p.xraw_off = g.xraw_off;
+    p.early = g.early;
+    p.rl = g.rl;
+    p.piece_chunks = g.piece_chunks;
+    p.x_bf16s = g.x_bf16s ? 1 : 0;
+    p.x_row_bytes = g.x_row_bytes;
+}
+
 int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void *ws, size_t ws_bytes,
              cudaStream_t stream, uint8_t *hq = nullptr)
 {
@@ -444,29 +473,7 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
             p.cnt = reinterpret_cast<int *>(static_cast<uint8_t *>(ws) + ((size_t)M * p.rows[0] * 4 + 15) / 16 * 16);
         }
     }
-    p.K = (int)K;
-    p.nb = (int)(K / QK);
-    p.nc = g.nc;
-    p.TPR = g.TPR;
-    p.RG = g.RG;
-    p.chunks_per_split = g.cps;
-    p.nstages = g.NS;
-    p.stage_rows = g.S;
-    p.row_stride = g.stride;
-    p.win_stages = g.win_stages;
-    p.part_off = g.part_off;
-    p.bar_off = g.bar_off;
-    p.ctas = g.ctas;
-    p.L = g.L;
-    p.wg = g.wg;
-    p.ng = g.ng;
-    p.x_off = g.x_off;
-    p.xraw_off = g.xraw_off;
-    p.early = g.early;
-    p.rl = g.rl;
-    p.piece_chunks = g.piece_chunks;
-    p.x_bf16s = g.x_bf16s ? 1 : 0;
-    p.x_row_bytes = g.x_row_bytes;
+    apply_plan(p, g, K);
     p.ws = (g.splits > 1) ? (float *)ws : nullptr;
     p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;
     const bool pdl = g_pdl.load() != 0;
@@ -823,6 +830,40 @@ int bqg_gemm_q8_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N
 
 int bqg_debug_q4_0_q8_1_block_dots(const void *Wp, const void *Xq, int32_t *dots, int64_t N, int64_t K,
                                    cudaStream_t stream)
+{
+    if (!Wp || !Xq || !dots || N < 0) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    if (!aligned16(Wp) || !aligned(Xq, 4) || !aligned(dots, 4)) return BQG_ERR_MISALIGNED;
+    DevInfo dev;
+    if (int st = current_device(&dev)) return st;
+    if (N == 0) return BQG_OK;
+    int dv = 0;
+    cudaGetDevice(&dv);
+    // the route bqg_gemv_q4_0_q8_1 takes at M = 1: the lanes-per-row kernel,
+    // else (staged activations too large) the K-slice kernel
+    GemvPlan g;
+    int st = plan_lpr(W_Q4_0, X_Q8_1, 1, N, K, 1, dev, dv, &g);
+    if (st == BQG_ERR_UNSUPPORTED_SHAPE)
+        return cuda_status(launch_block_dots(Wp, Xq, dots, N, K, repacked_row_bytes(BQG_Q4_0, K), stream));
+    if (st) return st;
+    GemvParams p{};
+    p.W[0] = (const uint8_t *)Wp;
+    p.rows[0] = N;
+    p.nmat = 1;
+    p.X = (const uint8_t *)Xq;
+    p.Nv = N;
+    p.row_bytes = repacked_row_bytes(BQG_Q4_0, K);
+    apply_plan(p, g, K);
+    p.epi = (g.splits > 1) ? EPI_PARTIAL : EPI_STORE;     // no output is written either way
+    p.dots = dots;
+    int occ = 0;
+    if (cudaError_t e = gemv_lpr_dots_run_q4_0_q8_1(p, g.grid, g.threads, g.smem, stream, &occ)) return cuda_status(e);
+    if (occ < 1) return BQG_ERR_UNSUPPORTED_SHAPE;
+    return cuda_status(gemv_lpr_dots_run_q4_0_q8_1(p, g.grid, g.threads, g.smem, stream, nullptr));
+}
+
+int bqg_debug_q4_0_q8_1_block_dots_kslice(const void *Wp, const void *Xq, int32_t *dots, int64_t N, int64_t K,
+                                          cudaStream_t stream)
 {
     if (!Wp || !Xq || !dots || N < 0) return BQG_ERR_INVALID_ARG;
     if (int st = check_k(K)) return st;

@@ -86,6 +86,9 @@ struct GemvParams {
     // block (zero between calls)
     uint8_t *hq;
     int *cnt;
+    // check instantiation only (q4_0 x q8_1, one activation row, one matrix):
+    // the integer block dots the kernel computes, rows x nb int32, row-major
+    int32_t *dots;
 };
 
 // One decode layer's three projection groups in one persistent launch
@@ -879,11 +882,13 @@ __device__ __forceinline__ int q4q8_sumi(const uint4 &c, const uint4 &xlo, const
 
 // acc[i][m] += dot(row i of the stage, activation row m) over tiles
 // [0, nt) of the stage (global tile tg + t); in the last tile only lanes
-// below `tail` hold a unit.
-template <int WF, int XF, int M, int RL>
+// below `tail` hold a unit.  DOTS (q4_0 x q8_1 check instantiation): the
+// integer dot of block b of stage row i < dots_rows is also stored at
+// dots[i * nb + b].
+template <int WF, int XF, int M, int RL, bool DOTS = false>
 __device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t *stage, int row_stride,
                                           const uint8_t *xs, int x_row_bytes, int ds_off, int tg, int nt, int tail,
-                                          int sub)
+                                          int sub, int32_t *dots = nullptr, int dots_rows = 0, int nb = 0)
 {
     constexpr int TW = TileTraits<WF>::TW;
     constexpr int TX = TileX<WF, XF>::TX;
@@ -1011,9 +1016,13 @@ __device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t 
                 const float2 ds = *reinterpret_cast<const float2 *>(xs + m * x_row_bytes + ds_off +
                                                                     ((tg + t) * 32 + sub) * 8);
 #pragma unroll
-                for (int i = 0; i < RL; i++)
-                    acc[i][m][0] = fmaf(d[i] * ds.x, (float)q4q8_sumi(c[i], xl, xh, __float_as_int(ds.y)),
-                                        acc[i][m][0]);
+                for (int i = 0; i < RL; i++) {
+                    const int sumi = q4q8_sumi(c[i], xl, xh, __float_as_int(ds.y));
+                    if constexpr (DOTS) {
+                        if (m == 0 && i < dots_rows) dots[(int64_t)i * nb + (tg + t) * 32 + sub] = sumi;
+                    }
+                    acc[i][m][0] = fmaf(d[i] * ds.x, (float)sumi, acc[i][m][0]);
+                }
             }
         } else if constexpr (XF == X_BF16) {
             // q4_0 against bf16 activations: unit = block sub; piece j
@@ -1110,9 +1119,12 @@ __device__ __forceinline__ void lpr_tiles(float (&acc)[RL][M][2], const uint8_t 
 // shared-memory activation reads per weight) fit in registers
 template <int M> struct LprThreads { static constexpr int value = (M >= 4) ? 256 : 384; };
 
-template <int WF, int XF, int M, int RL>
+// DOTS: the check instantiation (q4_0 x q8_1, M = 1, one matrix) that also
+// stores every integer block dot in p.dots and writes no output.
+template <int WF, int XF, int M, int RL, bool DOTS = false>
 __global__ void __launch_bounds__(LprThreads<M>::value, 2) gemv_lpr_kernel(const GemvParams p)
 {
+    static_assert(!DOTS || (WF == W_Q4_0 && XF == X_Q8_1 && M == 1), "block dots: q4_0 x q8_1, one row");
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
     constexpr int CPT = TileTraits<WF>::CPT;
@@ -1246,8 +1258,15 @@ __global__ void __launch_bounds__(LprThreads<M>::value, 2) gemv_lpr_kernel(const
             const int tg = ca / CPT;                                 // first tile (global) of the piece
             const int nt = (cb - ca + CPT - 1) / CPT;
             const int tail = min(32, units - 32 * (tg + nt - 1));   // units in the piece's last tile
-            lpr_tiles<WF, XF, M, RL>(acc, smem + (warp * D + d) * stage_bytes, row_stride, xs, x_row_bytes, ds_off, tg,
-                                     nt, tail, lane);
+            if constexpr (DOTS) {
+                const int64_t vb = v0 + (int64_t)(warp + NW * bl) * RL;      // first row of the stage
+                lpr_tiles<WF, XF, M, RL, true>(acc, smem + (warp * D + d) * stage_bytes, row_stride, xs, x_row_bytes,
+                                               ds_off, tg, nt, tail, lane, p.dots + vb * p.nb,
+                                               (int)(v1 - vb < RL ? v1 - vb : RL), p.nb);
+            } else {
+                lpr_tiles<WF, XF, M, RL>(acc, smem + (warp * D + d) * stage_bytes, row_stride, xs, x_row_bytes, ds_off,
+                                         tg, nt, tail, lane);
+            }
         }
         // the warp is done with this slot: refill it with the warp's stage t + D
         __syncwarp();
@@ -1287,7 +1306,7 @@ __global__ void __launch_bounds__(LprThreads<M>::value, 2) gemv_lpr_kernel(const
             continue;
         }
         if (lane != 0 || !ok) continue;
-        {
+        if constexpr (!DOTS) {
 #pragma unroll
             for (int i = 0; i < RL; i++) {
                 const int64_t v = staged_vrow(p, vb, RL, i);
@@ -1314,11 +1333,11 @@ __global__ void __launch_bounds__(LprThreads<M>::value, 2) gemv_lpr_kernel(const
     if (swiglu && p.hq) swiglu_q8_1_finish(p, M, v0 >> 1, v1 >> 1, 0, warp, NW, lane);
 }
 
-template <int WF, int XF, int M, int RL>
+template <int WF, int XF, int M, int RL, bool DOTS = false>
 __host__ cudaError_t gemv_lpr_launch_one(const GemvParams &p, dim3 grid, int threads, size_t smem,
                                          cudaStream_t stream, bool pdl, int *occupancy)
 {
-    auto kern = gemv_lpr_kernel<WF, XF, M, RL>;
+    auto kern = gemv_lpr_kernel<WF, XF, M, RL, DOTS>;
     if (occupancy) {
         int dev = 0, optin = 0;
         cudaFuncAttributes fa;
@@ -1366,6 +1385,20 @@ __host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, in
         BQG_LPR(XF, 4, 1) BQG_LPR(XF, 4, 2) BQG_LPR(XF, 8, 1) BQG_LPR(XF, 8, 2)
     }
 #undef BQG_LPR
+    return cudaErrorInvalidValue;
+}
+
+// The check instantiation of the q4_0 x q8_1 kernel at M = 1 (every rows-per-
+// lane choice the planner can make for it): same staging, stream and dot
+// routine as the GEMV, plus the integer block dots in p.dots.  With
+// `occupancy` set it only prepares the kernel (its shared-memory limit) and
+// reports its occupancy.
+__host__ inline cudaError_t gemv_lpr_dots_dispatch(const GemvParams &p, dim3 grid, int threads, size_t smem,
+                                                   cudaStream_t stream, int *occupancy)
+{
+    if (p.rl == 1) return gemv_lpr_launch_one<W_Q4_0, X_Q8_1, 1, 1, true>(p, grid, threads, smem, stream, false, occupancy);
+    if (p.rl == 2) return gemv_lpr_launch_one<W_Q4_0, X_Q8_1, 1, 2, true>(p, grid, threads, smem, stream, false, occupancy);
+    if (p.rl == 4) return gemv_lpr_launch_one<W_Q4_0, X_Q8_1, 1, 4, true>(p, grid, threads, smem, stream, false, occupancy);
     return cudaErrorInvalidValue;
 }
 

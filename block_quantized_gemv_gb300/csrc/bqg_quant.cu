@@ -306,7 +306,9 @@ __global__ void __launch_bounds__(256) copy_sm_kernel(const uint4 *__restrict__ 
 }
 
 // The exact per-block integer dots of q4_0 x q8_1 (one activation row),
-// computed with the GEMV's own device routine (q4_0_q8_1_sumi).
+// computed with the K-slice kernel's routine (q4_0_q8_1_sumi on the
+// operands as that kernel loads them: the q8_1 block through load_x, the
+// code chunk of the repacked row).
 __global__ void __launch_bounds__(256) block_dots_kernel(const uint8_t *__restrict__ Wp, const uint8_t *__restrict__ Xq,
                                                          int32_t *__restrict__ dots, int64_t N, int nb, int64_t row_bytes,
                                                          int K)

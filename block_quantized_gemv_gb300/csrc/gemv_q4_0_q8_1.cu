@@ -13,5 +13,10 @@ cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &p, int M, dim3 grid, int th
 {
     return gemv_lpr_dispatch<W_Q4_0, X_Q8_1>(p, M, grid, threads, smem, stream, pdl, occupancy);
 }
+cudaError_t gemv_lpr_dots_run_q4_0_q8_1(const GemvParams &p, dim3 grid, int threads, size_t smem, cudaStream_t stream,
+                                        int *occupancy)
+{
+    return gemv_lpr_dots_dispatch(p, grid, threads, smem, stream, occupancy);
+}
 int gemv_x_stage_bytes_q4_0_q8_1(int nc, int nb, int) { return x_stage_row_bytes<W_Q4_0, X_Q8_1>(nc, nb); }
 }  // namespace bqg

@@ -170,7 +170,10 @@ int bqg_gemv_q4_0_q8_1(const void *Wp, const void *Xq, float *Y, int M, int64_t 
  * holds until the process exits.
  *  - The first call on each device looks up the array's device address (a
  *    synchronous runtime call); make that first call before any stream
- *    capture.
+ *    capture.  The address is kept for the life of the process: a
+ *    cudaDeviceReset of that device afterwards (which reloads the library's
+ *    device image, perhaps elsewhere) leaves it stale, so this entry point
+ *    must not be called on a device after that device has been reset.
  *  - A shape whose split-K partials would not fit the array returns
  *    BQG_ERR_WORKSPACE and launches nothing.
  *  - Every call shares the array.  Nothing in it has to start at zero (a
@@ -263,11 +266,28 @@ int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N
 int bqg_gemm_q8_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
                        void *ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Debug export: the exact per-block integer dots of q4_0 x q8_1 for one
- * activation row, computed by the same device routine as the GEMV.
- * dots: N x K/32 int32, row-major (4-byte alignment is enough). */
+/* Check export: the exact per-block integer dots
+ *     dots[n, b] = sum_{i<32} (qw[n, 32b+i] - 8) * qx[32b+i]
+ * of q4_0 x q8_1 for one activation row (the integer-dot Q4_0 x Q8_1
+ * matvec of "rx-6700xt-llama2-decode", Approach & Methodology), exactly as
+ * bqg_gemv_q4_0_q8_1 computes them at M = 1 on this device: a check
+ * instantiation of the GEMV's own kernel for the plan that call would use
+ * (same staging of the activation row, same weight stream and dot routine;
+ * it writes the dots instead of the outputs), or, for the shapes that call
+ * serves with the K-slice kernel, that kernel's routine.
+ * Wp: repacked q4_0 N x K; Xq: K/32 q8_1 blocks (4-byte alignment is
+ * enough); dots: N x K/32 int32, row-major (4-byte alignment).  |dot| <=
+ * 32 * 8 * 127.  Errors as bqg_gemv_q4_0_q8_1. */
 int bqg_debug_q4_0_q8_1_block_dots(const void *Wp, const void *Xq, int32_t *dots, int64_t N,
                                    int64_t K, cudaStream_t stream);
+
+/* The same dots from the K-slice kernel's routine (q4_0_q8_1_sumi on the
+ * operands as that kernel loads them), whatever the shape: the routine the
+ * GEMV entry points use where the lanes-per-row kernel's staged
+ * activations do not fit (for example M = 8 at K = 11008).  Arguments and
+ * errors as bqg_debug_q4_0_q8_1_block_dots. */
+int bqg_debug_q4_0_q8_1_block_dots_kslice(const void *Wp, const void *Xq, int32_t *dots, int64_t N,
+                                          int64_t K, cudaStream_t stream);
 
 /* ---- utilities -------------------------------------------------------- */
 

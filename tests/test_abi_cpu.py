@@ -126,3 +126,10 @@ def test_no_device_is_an_error_not_a_fallback(L):
 def test_pdl_switch_roundtrip(L):
     prev = bqg.set_pdl(True)
     assert bqg.set_pdl(prev) is True
+
+
+def test_tensor_on_another_device_is_refused():
+    # the binding launches on the current device; a tensor elsewhere is an error, not a launch
+    bqg.check_device(0, 0, "X")
+    with pytest.raises(ValueError, match="cuda:1"):
+        bqg.check_device(1, 0, "X")

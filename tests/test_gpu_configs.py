@@ -95,11 +95,13 @@ def test_c3_decode_layer(ora):
     assert np.array_equal(hq.cpu().numpy().reshape(-1), hq_ref.reshape(-1))
     Yr, Ar = ora.gemv(Q4_0, canon["d"], Q8_1, hq_ref, 1, K, Nff, nthreads=16)
     check_close(Y, Yr, Ar, "C3 down")
-    # per-block integer dots of the down projection, bit-exact
-    dots = bqg.debug_q4_0_q8_1_block_dots(Wp["d"], hq, K, Nff)
+    # per-block integer dots of the down projection, bit-exact, from the
+    # GEMV's own kernel and plan and from the K-slice routine
     rows = np.arange(0, K, 97)
     want = ora.block_dots_q4_0_q8_1(canon["d"].reshape(K, -1)[rows], hq_ref, rows.size, Nff)
-    assert np.array_equal(dots.cpu().numpy()[rows], want)
+    for fn in (bqg.debug_q4_0_q8_1_block_dots, bqg.debug_q4_0_q8_1_block_dots_kslice):
+        dots = fn(Wp["d"], hq, K, Nff)
+        assert np.array_equal(dots.cpu().numpy()[rows], want), fn.__name__
 
 
 @pytest.mark.parametrize("M", [1, 2, 4, 8])

@@ -89,3 +89,20 @@ def test_gemv_degenerate_blocks_and_a_zero_row(ora, fmt, xf, M):
     y = Y.cpu()
     assert not y[1].any(), "an all-zero activation row must give exact zeros"
     assert not y[:, 0].any() and not y[:, 1].any(), "rows with zero scales must give exact zeros"
+
+
+def test_tensor_on_another_device_is_refused_before_launch(monkeypatch):
+    """The binding launches on the current device: a tensor that lives on
+    another one is refused (ValueError) before anything is enqueued.  With
+    one GPU the mismatch is made by pretending the current device is 1."""
+    N, K = 64, 256
+    W = torch.zeros(bqg.repacked_size(bqg.BF16, N, K), dtype=torch.uint8, device="cuda")
+    X = torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
+    Y = torch.full((1, N), 7.0, device="cuda")
+    torch.cuda.synchronize()
+    monkeypatch.setattr(bqg, "_current_device", lambda: 1)
+    with pytest.raises(ValueError, match="current device is cuda:1"):
+        bqg.gemv_bf16(W, X, N, K, out=Y)
+    monkeypatch.undo()
+    torch.cuda.synchronize()
+    assert torch.all(Y == 7.0)          # nothing ran

@@ -126,12 +126,45 @@ def test_repack_bitexact_and_roundtrip(ora, fmt, N, K):
     assert np.array_equal(ora.unrepack(fmt, packed, N, K), np.ascontiguousarray(canon).reshape(-1).view(np.uint8))
 
 
-@pytest.mark.parametrize("N,K", [(8, 64), (33, 1056), (256, 4096), (16, 11008)])
-def test_block_dots_bitexact(ora, N, K):
+def plant_extreme_blocks(canon, xq, N, K):
+    """Blocks at the ends of the integer range, written as bytes: weight codes
+    all 0 (q - 8 = -8), all 15 (+7), and the two nibble halves apart (0x0f,
+    0xf0), against activation codes all +127, all -127 and alternating +-127
+    (|sum| up to 32 * 8 * 127).  Scales 1.0 (fp16 0x3c00); the q8_1 s field
+    is fp16(d * sum q)."""
+    nb = K // 32
+    W = canon.reshape(N, nb, 18)
+    X = xq.reshape(nb, 36)
+    patterns = [0x00, 0xFF, 0x0F, 0xF0]
+    for r in range(min(N, 4)):
+        for b in range(min(nb, 4)):
+            W[r, b, 0:2] = (0x00, 0x3C)
+            W[r, b, 2:] = patterns[(r + b) % 4]
+    xcodes = [np.full(32, 127), np.full(32, -127), np.where(np.arange(32) % 2, 127, -127), np.full(32, 127)]
+    for b in range(min(nb, 4)):
+        q = xcodes[b].astype(np.int8)
+        X[b, 0:2] = (0x00, 0x3C)
+        X[b, 2:4] = np.array([q.astype(np.int64).sum()], dtype=np.float16).view(np.uint8)   # exact: |s| <= 4064
+        X[b, 4:] = q.view(np.uint8)
+    return canon, xq
+
+
+@pytest.mark.parametrize("route", ["gemv", "kslice"])
+@pytest.mark.parametrize("N,K", [(8, 64), (33, 1056), (256, 4096), (16, 11008), (4096, 11008), (5, 65536)])
+def test_block_dots_bitexact(ora, route, N, K):
+    """The int32 block dots sum (qw - 8) qx, bit-exact with the oracle, from
+    the GEMV's own lanes-per-row kernel (route "gemv": the plan
+    bqg_gemv_q4_0_q8_1 uses at M = 1) and from the K-slice kernel's routine."""
     _, canon = make_weights(ora, Q4_0, N, K, seed=3)
     xq = ora.quantize(Q8_1, synth.rms_normalised_f32(1, K, seed=4))
-    dots = bqg.debug_q4_0_q8_1_block_dots(gpu_repacked(Q4_0, canon, N, K), synth.u8_tensor(xq), N, K)
-    assert np.array_equal(dots.cpu().numpy(), ora.block_dots_q4_0_q8_1(canon, xq, N, K))
+    canon, xq = plant_extreme_blocks(canon, xq, N, K)
+    fn = bqg.debug_q4_0_q8_1_block_dots if route == "gemv" else bqg.debug_q4_0_q8_1_block_dots_kslice
+    out = torch.full((N, K // 32), -(2 ** 31), dtype=torch.int32, device="cuda")   # unwritten dots fail
+    dots = fn(gpu_repacked(Q4_0, canon, N, K), synth.u8_tensor(xq), N, K, out=out).cpu().numpy()
+    want = ora.block_dots_q4_0_q8_1(canon, xq, N, K)
+    if min(N, K // 32) >= 2:
+        assert want[0, 0] == -32 * 8 * 127 and want[1, 0] == 32 * 7 * 127     # the planted extremes arrived
+    assert np.array_equal(dots, want)
 
 
 # ---------------------------------------------------------------------------
@@ -179,10 +212,31 @@ def test_gemv_q4_0_q8_1(ora, M, N, K):
     run_gemv(ora, Q4_0, Q8_1, M, N, K, seed=N + K + M)
 
 
-def test_gemv_q4_0_q8_1_float_is_the_exact_integer_dots_scaled(ora):
-    # per-block float contribution = (d_w * d_x) * sumi with sumi exact
-    N, K = 64, 1024
-    run_gemv(ora, Q4_0, Q8_1, 1, N, K, seed=5)
+@pytest.mark.parametrize("N,K", [(64, 1024), (1000, 4096), (130, 11008)])
+def test_gemv_q4_0_q8_1_float_is_the_exact_integer_dots_scaled(ora, N, K):
+    """Each output is sum_b fp32(d_w d_x) * sumi_b with sumi_b the exact
+    integer dot: against that sum (fp64, from the oracle's dots and scales)
+    the GPU may differ only by fp32 accumulation, |err| <= (nb + 2) 2^-24
+    sum_b |fp32(d_w d_x) sumi_b| -- far inside the benchmark spec's bound, so a
+    wrong integer would show."""
+    _, canon = make_weights(ora, Q4_0, N, K, seed=5)
+    xq = ora.quantize(Q8_1, synth.rms_normalised_f32(1, K, seed=6))
+    Wp = gpu_repacked(Q4_0, canon, N, K)
+    Y = nan_like((1, N))
+    bqg.gemv_q4_0_q8_1(Wp, synth.u8_tensor(xq).view(1, -1), N, K, out=Y,
+                       ws=bqg.workspace(bqg.OP_GEMV_Q4_0_Q8_1, 1, N, K))
+    torch.cuda.synchronize()
+    nb = K // 32
+    dots = ora.block_dots_q4_0_q8_1(canon, xq, N, K).astype(np.float64)
+    dw = canon.reshape(N, nb, 18)[:, :, 0:2].copy().view(np.float16).reshape(N, nb).astype(np.float32)
+    dx = xq.reshape(nb, 36)[:, 0:2].copy().view(np.float16).reshape(nb).astype(np.float32)
+    scale = (dw * dx[None, :]).astype(np.float64)           # the fp32 product, rounded as the kernel rounds it
+    terms = scale * dots
+    want = terms.sum(axis=1)
+    bound = (nb + 2) * 2.0 ** -24 * np.abs(terms).sum(axis=1) + 1e-30
+    y = Y.cpu().double().numpy()[0]
+    assert np.all(np.isfinite(y))
+    assert np.all(np.abs(y - want) <= bound), f"max err/bound {np.max(np.abs(y - want) / bound):.3g}"
 
 
 @pytest.mark.parametrize("fmt,xf", [(BF16, BF16), (Q8_0, BF16), (Q4_0, Q8_1), (Q4_0, BF16)])
