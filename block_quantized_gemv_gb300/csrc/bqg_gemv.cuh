@@ -1191,14 +1191,27 @@ __global__ void __launch_bounds__(LprThreads<M>::value, 2) gemv_lpr_kernel(const
     if (lane == 0)
         for (; issued < early; issued++) issue(issued, issued);
 
+    // The activation rows may still be written by the previous grid, so they
+    // are read only after the wait below; but their lines can be brought into
+    // L2 now.  L2 is the point of coherence for the SMs' writes, so a line
+    // fetched early still returns the previous grid's data after the wait,
+    // and the copy after the wait then costs an L2 hit instead of a loaded
+    // HBM round trip (measured: -0.2 to -0.4 us per call for the quantized
+    // formats; nothing for bf16 weights, which skip it).  The span is the
+    // 16-byte-aligned one the copy below reads.
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(p.X);
+    const int xoff = (int)(xa & 15);
+    if constexpr (WF != W_BF16) {
+        if (tid == 32)
+            prefetch_l2_bulk(reinterpret_cast<const void *>(xa - xoff),
+                             (uint32_t)((xoff + M * x_src_row_bytes<XF>(p) + 15) & ~15ll));
+    }
     pdl_wait();
     pdl_launch_dependents();
     // The activation rows come in one bulk copy, requested before the rest of
     // the weight stream so that they do not queue behind it.  The copy covers
     // the 16-byte-aligned span around X (at most 15 bytes either side, which
     // never crosses a page), as bulk copies need 16-byte alignment.
-    const uintptr_t xa = reinterpret_cast<uintptr_t>(p.X);
-    const int xoff = (int)(xa & 15);
     if constexpr (XF == X_BF16) {
         // bf16 rows (16-byte aligned) straight into their staged rows
         if (tid == 0) {
