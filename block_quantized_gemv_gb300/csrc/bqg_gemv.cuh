@@ -1401,20 +1401,6 @@ __host__ cudaError_t gemv_lpr_dispatch(const GemvParams &p, int M, dim3 grid, in
     return cudaErrorInvalidValue;
 }
 
-// The check instantiation of the q4_0 x q8_1 kernel at M = 1 (every rows-per-
-// lane choice the planner can make for it): same staging, stream and dot
-// routine as the GEMV, plus the integer block dots in p.dots.  With
-// `occupancy` set it only prepares the kernel (its shared-memory limit) and
-// reports its occupancy.
-__host__ inline cudaError_t gemv_lpr_dots_dispatch(const GemvParams &p, dim3 grid, int threads, size_t smem,
-                                                   cudaStream_t stream, int *occupancy)
-{
-    if (p.rl == 1) return gemv_lpr_launch_one<W_Q4_0, X_Q8_1, 1, 1, true>(p, grid, threads, smem, stream, false, occupancy);
-    if (p.rl == 2) return gemv_lpr_launch_one<W_Q4_0, X_Q8_1, 1, 2, true>(p, grid, threads, smem, stream, false, occupancy);
-    if (p.rl == 4) return gemv_lpr_launch_one<W_Q4_0, X_Q8_1, 1, 4, true>(p, grid, threads, smem, stream, false, occupancy);
-    return cudaErrorInvalidValue;
-}
-
 // Split-K finish: Y = sum over splits (in split order) of the partials,
 // then the same epilogue as the single-pass kernel.
 static __global__ void __launch_bounds__(256) gemv_splitk_reduce(const GemvParams p, int M, int splits, int final_epi)
