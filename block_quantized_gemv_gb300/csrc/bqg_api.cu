@@ -420,6 +420,15 @@ size_t swiglu_q8_1_staging(int M, int64_t N)
     return ((size_t)M * N * 4 + 15) / 16 * 16 + (size_t)M * (N / 32) * 4;
 }
 
+// Does the lanes-per-row plan fit gemv_lpr_rows_kernel: one matrix, no
+// split of K, each stage whole rows, outputs stored as they are?
+bool rows_kernel_applies(const GemvPlan &g, const GemvParams &p)
+{
+    static const bool off = env_int("BQG_NO_ROWS_KERNEL", 0) != 0;
+    return !off && g.lpr && g.splits == 1 && p.nmat == 1 && p.epi == EPI_STORE && !p.hq &&
+           g.piece_chunks >= g.nc;
+}
+
 // The plan's geometry in the kernel parameters.
 void apply_plan(GemvParams &p, const GemvPlan &g, int64_t K)
 {
@@ -476,6 +485,7 @@ int run_gemv(int wf, int xf, GemvParams p, int M, int64_t K, int final_epi, void
     apply_plan(p, g, K);
     p.ws = (g.splits > 1) ? (float *)ws : nullptr;
     p.epi = (g.splits > 1) ? EPI_PARTIAL : final_epi;
+    p.rows_kernel = rows_kernel_applies(g, p) ? 1 : 0;
     const bool pdl = g_pdl.load() != 0;
     cudaError_t e = g.lpr ? lpr_runner(wf, xf)(p, M, g.grid, g.threads, g.smem, stream, pdl, nullptr)
                           : runner(wf, xf)(p, M, g.C, g.grid, g.threads, g.smem, stream, pdl, nullptr);
@@ -856,6 +866,7 @@ int bqg_debug_q4_0_q8_1_block_dots(const void *Wp, const void *Xq, int32_t *dots
     apply_plan(p, g, K);
     p.epi = (g.splits > 1) ? EPI_PARTIAL : EPI_STORE;     // no output is written either way
     p.dots = dots;
+    p.rows_kernel = rows_kernel_applies(g, p) ? 1 : 0;    // the kernel bqg_gemv_q4_0_q8_1 would run
     int occ = 0;
     if (cudaError_t e = gemv_lpr_dots_run_q4_0_q8_1(p, g.grid, g.threads, g.smem, stream, &occ)) return cuda_status(e);
     if (occ < 1) return BQG_ERR_UNSUPPORTED_SHAPE;

@@ -204,17 +204,18 @@ __device__ __forceinline__ uint4 dequant8_q8(uint32_t w0, uint32_t w1, float d)
 
 // A dequantizing thread's weight block, read from the raw group staged in
 // shared memory: `codes` is the group's 128 x 128-byte box (128-byte swizzle:
-// 16-byte chunk c of row r sits at chunk c ^ (r & 7)), `scales` the 128 x
-// 16-byte scale box, b8 the block within the group (0..7).
+// 16-byte chunk c of row r sits at chunk c ^ (r & 7)), b8 the block within
+// the group (0..7), d its scale.  The scales come from the group's 128 x
+// 16-byte scale box, each thread reading its row's 16 bytes in one load (a
+// warp's 32 rows are then 512 contiguous bytes: no bank conflict, where one
+// 2-byte load per block at a 16-byte row stride was a 4-way conflict).
 template <int WF> struct BlockCodes;
 template <> struct BlockCodes<BQG_Q4_0> {
     static constexpr int TILE = Q4_0_TILE, SCALE_OFF = 512;
     // block elements 0..31 -> v[0..3] (8 each): low nibbles are 0..15, high 16..31
-    static __device__ __forceinline__ void dequant(const uint8_t *codes, const uint8_t *scales, int r, int b8,
-                                                   uint4 (&v)[4])
+    static __device__ __forceinline__ void dequant(const uint8_t *codes, float d, int r, int b8, uint4 (&v)[4])
     {
         const uint4 c = *reinterpret_cast<const uint4 *>(codes + r * 128 + ((b8 ^ (r & 7)) << 4));
-        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(scales + r * 16 + 2 * b8));
         v[0] = dequant8(c.x, c.y, 0, d);
         v[1] = dequant8(c.z, c.w, 0, d);
         v[2] = dequant8(c.x, c.y, 4, d);
@@ -223,6 +224,8 @@ template <> struct BlockCodes<BQG_Q4_0> {
 };
 template <> struct BlockCodes<BQG_Q8_0> {
     static constexpr int TILE = Q8_0_TILE, SCALE_OFF = 1024;
+    // (q8_0 keeps one 2-byte scale load per block: measured faster for it, 73.9
+    // against 75.6-77.5 us for the variants at M = 512 N = 14336 K = 4096)
     static __device__ __forceinline__ void dequant(const uint8_t *codes, const uint8_t *scales, int r, int b8,
                                                    uint4 (&v)[4])
     {
@@ -417,6 +420,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
         int it = 0;       // global k-step counter (A slot ring)
         int gi = 0;       // global raw-group counter (raw ring)
         bool ok = true;
+        uint4 sc = make_uint4(0, 0, 0, 0);   // this row's eight fp16 scales of the current raw group
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
             for (int k = 0; k < nk && ok; k++) {
                 const int kq = k % RAW_STEPS;
@@ -424,6 +428,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
                 if (kq == 0) {
                     const bool raw_ready = mbar_wait_spin(bar_rawf(j), (gi / NRAW) & 1);
                     if (!__all_sync(0xffffffffu, raw_ready)) { fail(); ok = false; break; }
+                    if constexpr (WF == BQG_Q4_0)
+                        sc = *reinterpret_cast<const uint4 *>(smem + SM::OFF_SCALES + j * RAW_SCALES + r * 16);
                 }
                 const int step = it + k;
                 const int s = step % NSTAGE;
@@ -436,11 +442,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
                 const bool half = (k == nk - 1) && (a.K % TK) != 0;
                 if (!(half && h == 1)) {
                     const uint8_t *codes = smem + SM::OFF_RAW + j * SM::RAW_GROUP;
-                    const uint8_t *scales = smem + SM::OFF_SCALES + j * RAW_SCALES;
                     uint4 v[4];
-                    BlockCodes<WF>::dequant(codes, scales, r, 4 * kq + 2 * h, v);
-                    tmem_st16_nowait(arow + s * A_COLS, v);
-                    BlockCodes<WF>::dequant(codes, scales, r, 4 * kq + 2 * h + 1, v);
+                    if constexpr (WF == BQG_Q4_0) {
+                        // blocks 4 kq + 2h and + 1: the two halves of scale word 2 kq + h
+                        const uint32_t sw = kq ? (h ? sc.w : sc.z) : (h ? sc.y : sc.x);
+                        BlockCodes<WF>::dequant(codes, half_bits_to_float(sw & 0xffffu), r, 4 * kq + 2 * h, v);
+                        tmem_st16_nowait(arow + s * A_COLS, v);
+                        BlockCodes<WF>::dequant(codes, half_bits_to_float(sw >> 16), r, 4 * kq + 2 * h + 1, v);
+                    } else {
+                        const uint8_t *scales = smem + SM::OFF_SCALES + j * RAW_SCALES;
+                        BlockCodes<WF>::dequant(codes, scales, r, 4 * kq + 2 * h, v);
+                        tmem_st16_nowait(arow + s * A_COLS, v);
+                        BlockCodes<WF>::dequant(codes, scales, r, 4 * kq + 2 * h + 1, v);
+                    }
                     tmem_st16_nowait(arow + s * A_COLS + 16, v);
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }

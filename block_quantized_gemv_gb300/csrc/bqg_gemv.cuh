@@ -81,6 +81,8 @@ struct GemvParams {
     int rl;                 // rows per lane (lanes-per-row kernel: 1, 2 or 4)
     int piece_chunks;       // chunks per K-piece (lanes-per-row kernel)
     int x_bf16s;            // lanes-per-row kernel at M = 1: bf16 activations staged as bf16
+    int rows_kernel;        // lanes-per-row plan served by gemv_lpr_rows_kernel (one matrix, whole rows,
+                            // no split, plain store)
     // SwiGLU with a q8_1 output: the blocks go to hq (M x rows[0]/32 blocks);
     // Y[0] is then an fp32 staging row set and cnt one arrival counter per
     // block (zero between calls)
@@ -1346,22 +1348,210 @@ __global__ void __launch_bounds__(LprThreads<M>::value, 2) gemv_lpr_kernel(const
     if (swiglu && p.hq) swiglu_q8_1_finish(p, M, v0 >> 1, v1 >> 1, 0, warp, NW, lane);
 }
 
+// ---------------------------------------------------------------------------
+// Lanes-per-row kernel, common case: one matrix, whole rows in every stage,
+// no split of K, plain store of the outputs (every single-matrix GEMV whose
+// staged rows fit a stage, which includes the decode and sweep shapes).  It
+// is gemv_lpr_kernel with the general paths taken out at compile time:
+// stage t of a warp is its block t (RL consecutive rows, one bulk copy), the
+// tiles of a stage are the same for every stage, and each block's outputs
+// are finished by a recursive-halving warp reduction whose holder lanes
+// store them.  Measured on the decode shapes, the bookkeeping of the general
+// kernel (piece arithmetic per stage, matrix and epilogue branches per row)
+// was a quarter to a half of all instructions issued.
+// DOTS: the check instantiation (q4_0 x q8_1, M = 1) that also stores every
+// integer block dot in p.dots and writes no output.
+// ---------------------------------------------------------------------------
+template <int WF, int XF, int M, int RL, bool DOTS = false>
+__global__ void __launch_bounds__(LprThreads<M>::value, 2) gemv_lpr_rows_kernel(const GemvParams p)
+{
+    static_assert(!DOTS || (WF == W_Q4_0 && XF == X_Q8_1 && M == 1), "block dots: q4_0 x q8_1, one row");
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_abort;
+    constexpr int CPT = TileTraits<WF>::CPT;
+    constexpr int V = RL * M;                      // outputs a warp finishes per block
+    using WR = WarpReduce<V>;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int NW = p.ng;                           // warps
+    const int D = p.nstages;                       // slots per warp
+    const uint32_t row_bytes = (uint32_t)p.row_bytes;
+    const uint32_t stage_bytes = RL * row_bytes;   // a stage is RL whole rows
+    uint8_t *xs = smem + p.x_off;
+    const uint32_t bar0 = smem_u32(smem + p.bar_off);
+
+    int64_t v0, v1;
+    cta_rows(p, v0, v1);
+    const int nrows = (int)(v1 - v0);
+    const int nrb = (nrows + RL - 1) / RL;
+    const int my_blocks = (warp < nrb) ? (nrb - 1 - warp) / NW + 1 : 0;
+    const uint32_t slot0 = smem_u32(smem) + (uint32_t)warp * (uint32_t)D * stage_bytes;
+    const uint32_t wbar = bar0 + 8 * warp * D;
+    const uint32_t xbar = bar0 + 8 * NW * D;
+    const uint8_t *wrow0 = p.W[0] + v0 * p.row_bytes;
+    // block b of this warp: rows r = (warp + NW b) RL .. + RL of the CTA's range
+    auto issue = [&](int b, int slot) {
+        const int r = (warp + NW * b) * RL;
+        const uint32_t n = (uint32_t)min(RL, nrows - r) * row_bytes;
+        mbar_arrive_expect_tx(wbar + 8 * slot, n);
+        bulk_g2s(slot0 + slot * stage_bytes, wrow0 + (int64_t)r * row_bytes, n, wbar + 8 * slot);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < NW * D; i++) mbar_init(bar0 + 8 * i, 1);
+        mbar_init(xbar, 1);
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    int issued = 0;
+    const int first = min(D, my_blocks);
+    const int early = min(first, p.early);
+    if (lane == 0)
+        for (; issued < early; issued++) issue(issued, issued);
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(p.X);
+    const int xoff = (int)(xa & 15);
+    if constexpr (WF != W_BF16) {
+        // see gemv_lpr_kernel: the activation lines enter L2 before the wait
+        if (tid == 32)
+            prefetch_l2_bulk(reinterpret_cast<const void *>(xa - xoff),
+                             (uint32_t)((xoff + M * x_src_row_bytes<XF>(p) + 15) & ~15ll));
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    if constexpr (XF == X_BF16) {
+        if (tid == 0) {
+            const uint32_t rb = (uint32_t)p.K * 2;
+            mbar_arrive_expect_tx(xbar, (uint32_t)M * rb);
+            for (int m = 0; m < M; m++)
+                bulk_g2s(smem_u32(xs + (size_t)m * p.x_row_bytes), p.X + (size_t)m * rb, rb, xbar);
+        }
+    } else {
+        const uint32_t xcopy = (uint32_t)((xoff + M * x_src_row_bytes<XF>(p) + 15) & ~15ll);
+        if (tid == 0) {
+            mbar_arrive_expect_tx(xbar, xcopy);
+            bulk_g2s(smem_u32(smem + p.xraw_off), reinterpret_cast<const void *>(xa - xoff), xcopy, xbar);
+        }
+    }
+    __syncthreads();
+    if (lane == 0)
+        for (; issued < first; issued++) issue(issued, issued);
+    const bool xok = mbar_wait_bounded(xbar, 0);
+    if (!xok) {
+        atomicExch(&g_gemv_error, 1);
+        s_abort = 1;
+    }
+    if constexpr (XF == X_BF16)
+        permute_x_bf16<WF>(p, xs, M, warp, NW, lane);
+    else
+        expand_x<WF, XF>(p, smem + p.xraw_off + xoff, xs, M, tid, blockDim.x);
+    __syncthreads();
+
+    // the same tiles in every stage: tiles 0 .. nt-1 of the row, the last one
+    // holding `tail` units
+    const int nt = (p.nc + CPT - 1) / CPT;
+    const int units = (WF == W_BF16) ? p.nc : p.nb;
+    const int tail = units - 32 * (nt - 1);
+    const int ds_off = ((p.nc + 31) / 32) * XPieces<WF, XF>::P * 512;
+    const int x_row_bytes = p.x_row_bytes;
+    const int64_t N = p.rows[0];
+    float *const ycta = p.Y[0] + v0;
+
+    int d = 0;
+    uint32_t ph = 0;
+    int waited = 0;
+    bool ok = !*(volatile int *)&s_abort;
+    for (int b = 0; b < my_blocks && ok; b++) {
+        if (mbar_wait_bounded(wbar + 8 * d, ph)) {
+            waited++;
+        } else {
+            atomicExch(&g_gemv_error, 1);
+            s_abort = 1;
+        }
+        ok = !*(volatile int *)&s_abort;
+        if (!ok) break;
+        const int r0 = (warp + NW * b) * RL;           // first row of the block, from v0
+        float acc[RL][M][2];
+#pragma unroll
+        for (int i = 0; i < RL; i++)
+#pragma unroll
+            for (int m = 0; m < M; m++) acc[i][m][0] = acc[i][m][1] = 0.f;
+        const uint8_t *stage = smem + (warp * D + d) * stage_bytes;
+        if constexpr (DOTS) {
+            lpr_tiles<WF, XF, M, RL, true>(acc, stage, (int)row_bytes, xs, x_row_bytes, ds_off, 0, nt, tail, lane,
+                                           p.dots + (v0 + r0) * p.nb, min(RL, nrows - r0), p.nb);
+        } else {
+            lpr_tiles<WF, XF, M, RL>(acc, stage, (int)row_bytes, xs, x_row_bytes, ds_off, 0, nt, tail, lane);
+        }
+        // the warp is done with this slot: refill it with its block b + D
+        __syncwarp();
+        if (lane == 0 && b + D < my_blocks) {
+            fence_proxy_async_smem();
+            issue(b + D, d);
+            issued++;
+        }
+        if (++d == D) { d = 0; ph ^= 1; }
+        if constexpr (!DOTS) {
+            // value i * M + m is row r0 + i, activation row m
+            float v[V];
+#pragma unroll
+            for (int i = 0; i < RL; i++)
+#pragma unroll
+                for (int m = 0; m < M; m++) v[i * M + m] = acc[i][m][0] + acc[i][m][1];
+            const float tot = WR::run(v, lane);
+            if (WR::is_holder(lane)) {
+                const int idx = WR::index_of_lane(lane);
+                const int i = idx / M, m = idx - (idx / M) * M;
+                if (r0 + i < nrows) ycta[(int64_t)m * N + r0 + i] = tot;
+            }
+        }
+    }
+    // after a timeout: do not leave while this CTA's copies are in flight
+    if (lane == 0) {
+        for (int t = waited; t < issued; t++)
+            mbar_wait_bounded(wbar + 8 * (t % D), (uint32_t)((t / D) & 1));
+    }
+    if (tid == 0 && !xok) mbar_wait_bounded(xbar, 0);
+}
+
+// Allow `kern` the largest dynamic shared memory (opt-in limit minus its
+// static shared memory); error if `smem` does not fit.
+template <typename Kern>
+__host__ cudaError_t lpr_allow_smem(Kern kern, size_t smem)
+{
+    int dev = 0, optin = 0;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+    if (e == cudaSuccess && smem + fa.sharedSizeBytes > (size_t)optin) return cudaErrorInvalidValue;
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+    return e;
+}
+
+// With `occupancy` set: prepare both lanes-per-row kernels of this
+// instantiation (their shared-memory limit) and report the smaller of their
+// occupancies; else launch the one p.rows_kernel selects.
 template <int WF, int XF, int M, int RL, bool DOTS = false>
 __host__ cudaError_t gemv_lpr_launch_one(const GemvParams &p, dim3 grid, int threads, size_t smem,
                                          cudaStream_t stream, bool pdl, int *occupancy)
 {
-    auto kern = gemv_lpr_kernel<WF, XF, M, RL, DOTS>;
+    auto general = gemv_lpr_kernel<WF, XF, M, RL, DOTS>;
+    auto rows = gemv_lpr_rows_kernel<WF, XF, M, RL, DOTS>;
+    auto kern = p.rows_kernel ? rows : general;
     if (occupancy) {
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
-        if (e == cudaSuccess && smem + fa.sharedSizeBytes > (size_t)optin) return cudaErrorInvalidValue;
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+        cudaError_t e = lpr_allow_smem(general, smem);
+        if (e == cudaSuccess) e = lpr_allow_smem(rows, smem);
+        int o1 = 0, o2 = 0;
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, general, threads, smem);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, rows, threads, smem);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, kern, threads, smem);
+        *occupancy = min(o1, o2);
+        return cudaSuccess;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
