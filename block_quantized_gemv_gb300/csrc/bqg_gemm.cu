@@ -53,14 +53,29 @@ constexpr int TN = 128;         // activation rows per unit (MMA N)
 constexpr int TK = 128;         // K per stage: two 128-byte swizzle atoms of bf16
 constexpr int XATOM = 64;       // K of one swizzle atom (one TMA box)
 constexpr int ATOM_BYTES = TN * XATOM * 2;    // 16 KiB
-constexpr int NSTAGE = 4;
 constexpr int TILE_BYTES = TN * TK * 2;       // 32 KiB activation tile
 constexpr int STAGE_BYTES = TILE_BYTES;
 constexpr int ACC_COLS = TN;                  // fp32 columns per accumulator
-constexpr int A_COL0 = 2 * ACC_COLS;          // first column of the A slots
-constexpr int A_COLS = TK / 2;                // 32-bit columns of one A slot (two bf16 each)
-constexpr int TMEM_COLS = 512;                // 2 accumulators + NSTAGE A slots
-static_assert(A_COL0 + NSTAGE * A_COLS <= TMEM_COLS, "tensor memory budget");
+constexpr int A_COLS = TK / 2;                // 32-bit columns of one bf16 A tile of a stage (two bf16 each)
+constexpr int TMEM_COLS = 512;                // accumulators + NSTAGE A slots
+constexpr int kGemmExactBelowK = 1024;        // K below which the weights are split into exact bf16 terms
+
+// Pipeline shape per number of bf16 terms a dequantized weight is split
+// into.  TERMS = 1: (q - 8) d or q d rounded once to bf16 (the prefill
+// config's dequantization).  TERMS = 2 (q4_0) / 3 (q8_0): the weight written
+// exactly as a sum of bf16 values (a 4-bit code times an fp16 scale has at
+// most 14 significant bits, an 8-bit code times one at most 19, and bf16
+// holds 8), one MMA per term into the same fp32 accumulator, so the GEMM is
+// exact up to fp32 accumulation.  Each A slot holds the stage's terms; the
+// tensor memory then allows fewer stages (and, at three terms, one
+// accumulator).
+template <int TERMS> struct Pipe {
+    static constexpr int NSTAGE = (TERMS == 1) ? 4 : 2;
+    static constexpr int NACC = (TERMS == 3) ? 1 : 2;
+    static constexpr int A_COL0 = NACC * ACC_COLS;        // first column of the A slots
+    static constexpr int SLOT_COLS = TERMS * A_COLS;      // one stage's A terms
+    static_assert(A_COL0 + NSTAGE * SLOT_COLS <= TMEM_COLS, "tensor memory budget");
+};
 constexpr int DQ_WARPS = 8;                   // dequantizing warps (1..8)
 constexpr int EPI_WARP0 = 1 + DQ_WARPS;       // epilogue warps 9..12
 constexpr int TMA_WARP = EPI_WARP0 + 4;       // activation loads: warp 13
@@ -70,8 +85,9 @@ constexpr int RAW_STEPS = 2;                  // stages per raw group: 8 blocks 
 constexpr int RAW_CODES = TM * 128;           // bytes of one 128-row x 128-byte code box
 constexpr int RAW_SCALES = TM * 16;           // bytes of one 128-row x 16-byte scale box
 
-// shared memory map (dynamic, 1024-byte aligned), per weight format
-template <int WF> struct GemmSmem {
+// shared memory map (dynamic, 1024-byte aligned), per weight format and
+// number of activation stages
+template <int WF, int NSTAGE> struct GemmSmem {
     static constexpr int CODE_BOXES = (WF == BQG_Q8_0) ? 2 : 1;   // q8_0: codes 0..15 and 16..31
     static constexpr int NRAW = (WF == BQG_Q8_0) ? 2 : 3;         // raw groups in flight
     static constexpr int RAW_GROUP = CODE_BOXES * RAW_CODES;
@@ -167,10 +183,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
-// 8 dequantized weights (q - 8) * d of one q4_0 word pair, as 4 bf16x2 words.
-// w0, w1 hold code bytes 4i..4i+7; `shift` 0 takes the low nibbles (elements
-// j), 4 the high nibbles (elements j + 16).
-__device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, int shift, float d)
+// Eight exact fp32 weights as TERMS bf16x2 quadruples: term 0 is each weight
+// rounded to nearest-even bf16, every further term the same rounding of what
+// is left (the subtraction is exact); with enough terms the sum of the terms
+// is the weight exactly.
+template <int TERMS>
+__device__ __forceinline__ void bf16_terms(float (&f)[8], uint4 (&t)[TERMS])
+{
+#pragma unroll
+    for (int j = 0; j < TERMS; j++) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+            if (j + 1 < TERMS) {
+                f[2 * i] = __fsub_rn(f[2 * i], __uint_as_float(w[i] << 16));
+                f[2 * i + 1] = __fsub_rn(f[2 * i + 1], __uint_as_float(w[i] & 0xffff0000u));
+            }
+        }
+        t[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// 8 dequantized weights (q - 8) * d of one q4_0 word pair, as TERMS bf16x2
+// quadruples.  w0, w1 hold code bytes 4i..4i+7; `shift` 0 takes the low
+// nibbles (elements j), 4 the high nibbles (elements j + 16).
+template <int TERMS>
+__device__ __forceinline__ void dequant8(uint32_t w0, uint32_t w1, int shift, float d, uint4 (&t)[TERMS])
 {
     constexpr float OFF = 8388608.0f + 8.0f;
     const uint32_t a = (w0 >> shift) & 0x0f0f0f0fu, b = (w1 >> shift) & 0x0f0f0f0fu;
@@ -181,13 +220,13 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, int shift, f
         fadd2(f[i], f[i + 1], -OFF);
         fmul2(f[i], f[i + 1], d);
     }
-    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                      pack_bf16x2(f[6], f[7]));
+    bf16_terms<TERMS>(f, t);
 }
 
 // 8 dequantized q8_0 weights q * d of one word pair (bytes = codes 4i..4i+7),
-// as 4 bf16x2 words
-__device__ __forceinline__ uint4 dequant8_q8(uint32_t w0, uint32_t w1, float d)
+// as TERMS bf16x2 quadruples
+template <int TERMS>
+__device__ __forceinline__ void dequant8_q8(uint32_t w0, uint32_t w1, float d, uint4 (&t)[TERMS])
 {
     constexpr float OFF = 8388608.0f + 128.0f;
     const uint32_t a = w0 ^ 0x80808080u, b = w1 ^ 0x80808080u;   // q + 128 as unsigned bytes
@@ -198,8 +237,7 @@ __device__ __forceinline__ uint4 dequant8_q8(uint32_t w0, uint32_t w1, float d)
         fadd2(f[i], f[i + 1], -OFF);
         fmul2(f[i], f[i + 1], d);
     }
-    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                      pack_bf16x2(f[6], f[7]));
+    bf16_terms<TERMS>(f, t);
 }
 
 // A dequantizing thread's weight block, read from the raw group staged in
@@ -212,31 +250,44 @@ __device__ __forceinline__ uint4 dequant8_q8(uint32_t w0, uint32_t w1, float d)
 template <int WF> struct BlockCodes;
 template <> struct BlockCodes<BQG_Q4_0> {
     static constexpr int TILE = Q4_0_TILE, SCALE_OFF = 512;
-    // block elements 0..31 -> v[0..3] (8 each): low nibbles are 0..15, high 16..31
-    static __device__ __forceinline__ void dequant(const uint8_t *codes, float d, int r, int b8, uint4 (&v)[4])
+    // block elements 0..31 -> v[term][0..3] (8 each): low nibbles are 0..15, high 16..31
+    template <int TERMS>
+    static __device__ __forceinline__ void dequant(const uint8_t *codes, float d, int r, int b8,
+                                                   uint4 (&v)[TERMS][4])
     {
         const uint4 c = *reinterpret_cast<const uint4 *>(codes + r * 128 + ((b8 ^ (r & 7)) << 4));
-        v[0] = dequant8(c.x, c.y, 0, d);
-        v[1] = dequant8(c.z, c.w, 0, d);
-        v[2] = dequant8(c.x, c.y, 4, d);
-        v[3] = dequant8(c.z, c.w, 4, d);
+        uint4 t[4][TERMS];
+        dequant8<TERMS>(c.x, c.y, 0, d, t[0]);
+        dequant8<TERMS>(c.z, c.w, 0, d, t[1]);
+        dequant8<TERMS>(c.x, c.y, 4, d, t[2]);
+        dequant8<TERMS>(c.z, c.w, 4, d, t[3]);
+#pragma unroll
+        for (int j = 0; j < TERMS; j++)
+#pragma unroll
+            for (int g = 0; g < 4; g++) v[j][g] = t[g][j];
     }
 };
 template <> struct BlockCodes<BQG_Q8_0> {
     static constexpr int TILE = Q8_0_TILE, SCALE_OFF = 1024;
     // (q8_0 keeps one 2-byte scale load per block: measured faster for it, 73.9
     // against 75.6-77.5 us for the variants at M = 512 N = 14336 K = 4096)
+    template <int TERMS>
     static __device__ __forceinline__ void dequant(const uint8_t *codes, const uint8_t *scales, int r, int b8,
-                                                   uint4 (&v)[4])
+                                                   uint4 (&v)[TERMS][4])
     {
         const int off = r * 128 + ((b8 ^ (r & 7)) << 4);
         const uint4 lo = *reinterpret_cast<const uint4 *>(codes + off);             // codes 0..15
         const uint4 hi = *reinterpret_cast<const uint4 *>(codes + RAW_CODES + off); // codes 16..31
         const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(scales + r * 16 + 2 * b8));
-        v[0] = dequant8_q8(lo.x, lo.y, d);
-        v[1] = dequant8_q8(lo.z, lo.w, d);
-        v[2] = dequant8_q8(hi.x, hi.y, d);
-        v[3] = dequant8_q8(hi.z, hi.w, d);
+        uint4 t[4][TERMS];
+        dequant8_q8<TERMS>(lo.x, lo.y, d, t[0]);
+        dequant8_q8<TERMS>(lo.z, lo.w, d, t[1]);
+        dequant8_q8<TERMS>(hi.x, hi.y, d, t[2]);
+        dequant8_q8<TERMS>(hi.z, hi.w, d, t[3]);
+#pragma unroll
+        for (int j = 0; j < TERMS; j++)
+#pragma unroll
+            for (int g = 0; g < 4; g++) v[j][g] = t[g][j];
     }
 };
 
@@ -249,13 +300,15 @@ struct GemmArgs {
     int tiles_n;            // N / TM
 };
 
-template <int WF>
+template <int WF, int TERMS>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                    const __grid_constant__ CUtensorMap cmap,
                                                                    const __grid_constant__ CUtensorMap smap,
                                                                    const GemmArgs a)
 {
-    using SM = GemmSmem<WF>;
+    using PP = Pipe<TERMS>;
+    constexpr int NSTAGE = PP::NSTAGE, NACC = PP::NACC, A_COL0 = PP::A_COL0, SLOT_COLS = PP::SLOT_COLS;
+    using SM = GemmSmem<WF, NSTAGE>;
     constexpr int OFF_STAGES = SM::OFF_STAGES, OFF_BARS = SM::OFF_BARS, OFF_TMEM_SLOT = SM::OFF_TMEM_SLOT;
     constexpr int OFF_FLAG = SM::OFF_FLAG, NRAW = SM::NRAW;
     extern __shared__ uint8_t smem_raw[];
@@ -317,9 +370,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
             int ucount = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ucount++) {
-                const int b = ucount & 1;
-                // the accumulator must have been read out (two units ago)
-                if (ucount >= 2 && !mbar_wait_spin(bar_acce(b), ((ucount >> 1) - 1) & 1)) { fail(); ok = false; break; }
+                const int b = ucount % NACC;
+                // the accumulator must have been read out (NACC units ago)
+                if (ucount >= NACC && !mbar_wait_spin(bar_acce(b), ((ucount / NACC) - 1) & 1)) {
+                    fail(); ok = false; break;
+                }
                 tc_fence_after();
                 const uint32_t dacc = tmem + b * ACC_COLS;
                 for (int k = 0; k < nk && ok; k++) {
@@ -331,15 +386,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
                     }
                     if (*abort_flag) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t aw = tmem + A_COL0 + s * A_COLS;                 // weights: MMA A (M = 128 rows)
+                    const uint32_t aw = tmem + A_COL0 + s * SLOT_COLS;              // weights: MMA A (M = 128 rows)
                     const uint32_t bx = sbase + OFF_STAGES + s * STAGE_BYTES;       // activations: MMA B (N = 128)
                     // a last stage of K = 64 (K % 128 == 64) holds one atom
                     const int nkk = (k == nk - 1 && (a.K % TK) != 0) ? XATOM / 16 : TK / 16;
 #pragma unroll
                     for (int kk = 0; kk < TK / 16; kk++) {
                         if (kk >= nkk) break;
-                        umma_bf16_ts(dacc, aw + kk * 8, sw128_desc(bx + (kk >> 2) * ATOM_BYTES + (kk & 3) * 32),
-                                     (k > 0 || kk > 0) ? 1u : 0u);
+                        const uint64_t bdesc = sw128_desc(bx + (kk >> 2) * ATOM_BYTES + (kk & 3) * 32);
+#pragma unroll
+                        for (int j = 0; j < TERMS; j++)      // the weight's bf16 terms, one MMA each
+                            umma_bf16_ts(dacc, aw + j * A_COLS + kk * 8, bdesc, (k > 0 || kk > 0 || j > 0) ? 1u : 0u);
                     }
                     umma_commit(bar_empty(s));               // stage s is free when these MMAs finish
                 }
@@ -417,6 +474,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
         const int r = quarter * 32 + lane;                   // weight row in the unit
         const int h = (warp - 1) >> 2;                       // which pair of the stage's four blocks
         const uint32_t arow = tmem + ((uint32_t)(quarter * 32) << 16) + A_COL0 + h * (A_COLS / 2);
+        auto store_terms = [&](uint32_t col, uint4 (&v)[TERMS][4]) {
+#pragma unroll
+            for (int j = 0; j < TERMS; j++) tmem_st16_nowait(col + j * A_COLS, v[j]);
+        };
         int it = 0;       // global k-step counter (A slot ring)
         int gi = 0;       // global raw-group counter (raw ring)
         bool ok = true;
@@ -442,20 +503,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
                 const bool half = (k == nk - 1) && (a.K % TK) != 0;
                 if (!(half && h == 1)) {
                     const uint8_t *codes = smem + SM::OFF_RAW + j * SM::RAW_GROUP;
-                    uint4 v[4];
+                    uint4 v[TERMS][4];
                     if constexpr (WF == BQG_Q4_0) {
                         // blocks 4 kq + 2h and + 1: the two halves of scale word 2 kq + h
                         const uint32_t sw = kq ? (h ? sc.w : sc.z) : (h ? sc.y : sc.x);
-                        BlockCodes<WF>::dequant(codes, half_bits_to_float(sw & 0xffffu), r, 4 * kq + 2 * h, v);
-                        tmem_st16_nowait(arow + s * A_COLS, v);
-                        BlockCodes<WF>::dequant(codes, half_bits_to_float(sw >> 16), r, 4 * kq + 2 * h + 1, v);
+                        BlockCodes<WF>::template dequant<TERMS>(codes, half_bits_to_float(sw & 0xffffu), r,
+                                                                4 * kq + 2 * h, v);
+                        store_terms(arow + s * SLOT_COLS, v);
+                        BlockCodes<WF>::template dequant<TERMS>(codes, half_bits_to_float(sw >> 16), r,
+                                                                4 * kq + 2 * h + 1, v);
                     } else {
                         const uint8_t *scales = smem + SM::OFF_SCALES + j * RAW_SCALES;
-                        BlockCodes<WF>::dequant(codes, scales, r, 4 * kq + 2 * h, v);
-                        tmem_st16_nowait(arow + s * A_COLS, v);
-                        BlockCodes<WF>::dequant(codes, scales, r, 4 * kq + 2 * h + 1, v);
+                        BlockCodes<WF>::template dequant<TERMS>(codes, scales, r, 4 * kq + 2 * h, v);
+                        store_terms(arow + s * SLOT_COLS, v);
+                        BlockCodes<WF>::template dequant<TERMS>(codes, scales, r, 4 * kq + 2 * h + 1, v);
                     }
-                    tmem_st16_nowait(arow + s * A_COLS + 16, v);
+                    store_terms(arow + s * SLOT_COLS + 16, v);
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
                 tc_fence_before();                             // tensor-memory writes -> the MMA thread
@@ -474,8 +537,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
         int ucount = 0;
         for (int u = blockIdx.x; u < a.units; u += gridDim.x, ucount++) {
             const int tn = u % a.tiles_n, tm = u / a.tiles_n;
-            const int b = ucount & 1;
-            if (*abort_flag || !mbar_wait_spin(bar_accf(b), (ucount >> 1) & 1)) { fail(); break; }
+            const int b = ucount % NACC;
+            if (*abort_flag || !mbar_wait_spin(bar_accf(b), (ucount / NACC) & 1)) { fail(); break; }
             tc_fence_after();
             const int n = tn * TM + quarter * 32 + lane;     // weight row = output column
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + b * ACC_COLS;
@@ -569,23 +632,41 @@ int gemm_bf16(int wf, const void *Wp, const void *X, float *Y, int M, int64_t N,
     a.K = (int)K;
     a.tiles_n = (int)(N / TM);
     a.units = a.tiles_n * (M / TN);
+    // Below K = 1024 a product of few terms can be dominated by one weight,
+    // and the one bf16 rounding of (q - 8) d (relative error up to 2^-9) can
+    // then exceed the parity bound 1e-3 sum |w x|; those calls split each
+    // weight exactly into bf16 terms (two for q4_0, three for q8_0).  From
+    // K = 1024 on, one rounding per weight (the config's bf16 dequantization).
+    const bool exact = K < kGemmExactBelowK;
     {
         std::lock_guard<std::mutex> lk(mu);
         static bool attr = false;
         if (!attr) {
-            if (cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q4_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     GemmSmem<BQG_Q4_0>::SMEM_BYTES) != cudaSuccess ||
-                cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q8_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     GemmSmem<BQG_Q8_0>::SMEM_BYTES) != cudaSuccess)
+            if (cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q4_0, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GemmSmem<BQG_Q4_0, Pipe<1>::NSTAGE>::SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q4_0, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GemmSmem<BQG_Q4_0, Pipe<2>::NSTAGE>::SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q8_0, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GemmSmem<BQG_Q8_0, Pipe<1>::NSTAGE>::SMEM_BYTES) != cudaSuccess ||
+                cudaFuncSetAttribute(gemm_bf16_kernel<BQG_Q8_0, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     GemmSmem<BQG_Q8_0, Pipe<3>::NSTAGE>::SMEM_BYTES) != cudaSuccess)
                 return BQG_ERR_CUDA;
             attr = true;
         }
     }
     const int grid = std::min(a.units, sms);
-    if (wf == BQG_Q8_0)
-        gemm_bf16_kernel<BQG_Q8_0><<<grid, NUM_THREADS, GemmSmem<BQG_Q8_0>::SMEM_BYTES, stream>>>(map, cmap, smap, a);
+    if (wf == BQG_Q8_0 && exact)
+        gemm_bf16_kernel<BQG_Q8_0, 3><<<grid, NUM_THREADS, GemmSmem<BQG_Q8_0, Pipe<3>::NSTAGE>::SMEM_BYTES, stream>>>(
+            map, cmap, smap, a);
+    else if (wf == BQG_Q8_0)
+        gemm_bf16_kernel<BQG_Q8_0, 1><<<grid, NUM_THREADS, GemmSmem<BQG_Q8_0, Pipe<1>::NSTAGE>::SMEM_BYTES, stream>>>(
+            map, cmap, smap, a);
+    else if (exact)
+        gemm_bf16_kernel<BQG_Q4_0, 2><<<grid, NUM_THREADS, GemmSmem<BQG_Q4_0, Pipe<2>::NSTAGE>::SMEM_BYTES, stream>>>(
+            map, cmap, smap, a);
     else
-        gemm_bf16_kernel<BQG_Q4_0><<<grid, NUM_THREADS, GemmSmem<BQG_Q4_0>::SMEM_BYTES, stream>>>(map, cmap, smap, a);
+        gemm_bf16_kernel<BQG_Q4_0, 1><<<grid, NUM_THREADS, GemmSmem<BQG_Q4_0, Pipe<1>::NSTAGE>::SMEM_BYTES, stream>>>(
+            map, cmap, smap, a);
     return cudaGetLastError() == cudaSuccess ? BQG_OK : BQG_ERR_CUDA;
 }
 

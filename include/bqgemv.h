@@ -253,16 +253,22 @@ int bqg_decode_layer_q4_0_q8_1(const void *xa, const void *xb, int x_dtype, cons
                                size_t ws_bytes, cudaStream_t stream);
 
 /* Prefill GEMM ("llama-3x-prompt-speed", "the tile"): each weight tile is
- * dequantized once to bf16 ((q-8)*d rounded to nearest-even bf16) into the
- * tensor memory the MMA reads and fed to the tensor cores with fp32
- * accumulation.  Wp: repacked q4_0 N x K; X: M x K bf16; Y: M x N fp32.
+ * dequantized once to bf16 into the tensor memory the MMA reads and fed to
+ * the tensor cores with fp32 accumulation.  For K >= 1024 each weight
+ * (q-8)*d is rounded once to nearest-even bf16 (relative error <= 2^-9 per
+ * weight); for K < 1024, where one large term can dominate a short sum and
+ * that rounding could exceed the library's parity bound 1e-3 * sum|w x|,
+ * each weight is written exactly as a sum of two bf16 terms, one MMA each.
+ * Wp: repacked q4_0 N x K; X: M x K bf16; Y: M x N fp32.
  * M a positive multiple of 128, N a multiple of 128, K a multiple of 64. */
 int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
                        void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* The same prefill GEMM with q8_0 weights (the q8_0 tile of
  * "llama-3x-prompt-speed", "the free 2x"): q * d rounded to nearest-even
- * bf16.  Wp: repacked q8_0 N x K; other arguments as bqg_gemm_q4_0_bf16. */
+ * bf16 for K >= 1024, and for K < 1024 written exactly as three bf16 terms
+ * (an 8-bit code times an fp16 scale has up to 19 significant bits).
+ * Wp: repacked q8_0 N x K; other arguments as bqg_gemm_q4_0_bf16. */
 int bqg_gemm_q8_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
                        void *ws, size_t ws_bytes, cudaStream_t stream);
 
