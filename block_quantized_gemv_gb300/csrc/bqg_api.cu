@@ -321,9 +321,9 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     // few KiB moved).
     g.L = 32;
     // measured on the decode and sweep shapes: two rows per lane for q4_0
-    // (q8_1 or bf16 activations) at M = 1, 2 and for bf16 weights at M = 2,
-    // one otherwise
-    int rl = ((M <= 2 && wf == W_Q4_0) || (M == 2 && wf == W_BF16)) ? 2 : 1;
+    // (q8_1 or bf16 activations) at M = 1 and for every format at M = 2, one
+    // otherwise (q8_0 at M = 1 below)
+    int rl = ((M == 1 && wf == W_Q4_0) || M == 2) ? 2 : 1;
     // q8_0 x bf16 at M = 1 (bf16-staged): two rows per lane (each activation
     // piece converted once for both rows), with one slot per warp when each
     // CTA has few rows (N = 4096: 13 per CTA) and two otherwise (measured at
@@ -358,11 +358,13 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     const int slots = (int)std::min<int64_t>(64, budget / stage);
     int ng = std::max(1, std::min(max_warps, slots / 2));
     int D = std::max(1, slots / ng);
-    // measured: q8_1 activations, q4_0 weights and M >= 2 gain more from
-    // more warps with one slot each than from double slots; bf16 and q8_0
-    // weights at M = 1 keep two
-    const bool one_slot = xf == X_Q8_1 || M >= 2 || wf == W_Q4_0 || q8_m1_few;
-    const int want_D = (force_D > 0) ? force_D : one_slot ? 1 : 0;
+    // measured: at M = 1 q8_1 activations and q4_0 weights gain more from more
+    // warps with one slot each than from double slots, bf16 and q8_0 weights
+    // keep two; at M = 2 and 4 two slots per warp win by 1-4 % on the sweep
+    // shape (q4_0 x bf16 at M = 2 excepted), at M = 8 one slot
+    const bool two_slots_m24 = (M == 2 || M == 4) && !(M == 2 && wf == W_Q4_0 && xf == X_BF16);
+    const bool one_slot = !two_slots_m24 && (xf == X_Q8_1 || M >= 2 || wf == W_Q4_0 || q8_m1_few);
+    const int want_D = (force_D > 0) ? force_D : one_slot ? 1 : two_slots_m24 ? 2 : 0;
     if (want_D > 0) { D = want_D; ng = std::max(1, std::min(max_warps, slots / D)); }
     g.ng = ng;
     g.NS = D;
