@@ -243,6 +243,7 @@ class GemvArm(Arm):
         op = {"bf16": bqg.OP_GEMV_BF16, "q8_0": bqg.OP_GEMV_Q8_0, "q4_0": bqg.OP_GEMV_Q4_0}[names[fmt]]
         if xfmt == bqg.Q8_1:
             op = bqg.OP_GEMV_Q4_0_Q8_1
+        self.route = bqg.ROUTE_NAMES[bqg.gemv_route(op, M, N, K)]
         for r in range(self.R):
             self.sets.append({"W": Wp if r == 0 else Wp.clone(), "X": X.clone(),
                               "Y": torch.empty((M, N), dtype=torch.float32, device="cuda"),
@@ -559,6 +560,8 @@ def arm_record(arm, t, peaks):
            "launches": calls * arm.launches_per_call, "clocks": t.get("clocks")}
     if getattr(arm, "vendor", False):
         rec["vendor"] = "library GEMV for context (cuBLAS through torch.matmul), not this repository's kernels"
+    if getattr(arm, "route", None):
+        rec["route"] = arm.route
     if rec["rejected"]:
         return rec
     us = t["seconds"] / calls * 1e6

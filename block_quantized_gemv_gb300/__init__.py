@@ -50,6 +50,7 @@ EXPORTS = {
     "bqg_debug_q4_0_q8_1_block_dots": (["p", "p", "p", "i64", "i64", "p"], "i"),
     "bqg_debug_q4_0_q8_1_block_dots_kslice": (["p", "p", "p", "i64", "i64", "p"], "i"),
     "bqg_workspace_size": (["i", "i", "i64", "i64"], "size"),
+    "bqg_gemv_route": (["i", "i", "i64", "i64", "p"], "i"),
     "bqg_last_device_error": (["p", "p"], "i"),
     "bqg_set_pdl": (["i"], "i"),
     "bqg_host_alias": (["p", "p"], "i"),
@@ -414,6 +415,18 @@ def workspace(op: int, M: int, N: int, K: int, device="cuda") -> torch.Tensor | 
     """A workspace for `op` (zero-filled, as the q8_1-output SwiGLU requires)."""
     n = workspace_size(op, M, N, K)
     return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
+
+
+ROUTE_K_SLICE, ROUTE_LANES_PER_ROW, ROUTE_LANES_PER_ROW_ROWS, ROUTE_TENSOR_CORE = 0, 1, 2, 3
+ROUTE_NAMES = {0: "k_slice", 1: "lanes_per_row", 2: "lanes_per_row_rows", 3: "tensor_core"}
+
+
+def gemv_route(op: int, M: int, N: int, K: int) -> int:
+    """Which kernel serves a GEMV call of this shape on the current device
+    (one of the ROUTE_* values)."""
+    out = ctypes.c_int(-1)
+    _check(load().bqg_gemv_route(op, M, N, K, ctypes.addressof(out)), "bqg_gemv_route")
+    return out.value
 
 
 def last_device_error(stream=None) -> int:

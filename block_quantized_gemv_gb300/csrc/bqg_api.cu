@@ -9,7 +9,10 @@
 #include <mutex>
 #include <tuple>
 
+#include <cudaTypedefs.h>
+
 #include "bqg_gemv.cuh"
+#include "bqg_gemv_mma.cuh"
 
 namespace bqg {
 cudaError_t gemv_run_bf16(const GemvParams &, int, int, dim3, int, size_t, cudaStream_t, bool, int *);
@@ -25,6 +28,11 @@ cudaError_t gemv_lpr_run_q8_0(const GemvParams &, int, dim3, int, size_t, cudaSt
 cudaError_t gemv_lpr_run_q4_0(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_lpr_run_q4_0_q8_1(const GemvParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_lpr_dots_run_q4_0_q8_1(const GemvParams &, dim3, int, size_t, cudaStream_t, int *);
+using MmaFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const MmaParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_mma_run_bf16(const CUtensorMap &, const CUtensorMap &, const MmaParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_mma_run_q8_0(const CUtensorMap &, const CUtensorMap &, const MmaParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_mma_run_q4_0(const CUtensorMap &, const CUtensorMap &, const MmaParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 int gemv_x_stage_bytes_bf16(int, int, int);
 int gemv_x_stage_bytes_q8_0(int, int, int);
 int gemv_x_stage_bytes_q4_0(int, int, int);
@@ -528,6 +536,131 @@ int check_k(int64_t K)
     return BQG_OK;
 }
 
+// The tensor-core route (bqg_gemv_mma.cuh): M = 4 or 8, bf16 activations,
+// one matrix, outputs stored as they are, staged activations within 80 KiB
+// (M K <= about 40960).  One CTA per SM, eight warps; as many slots per warp
+// (at most four) as the shared memory left by the staged activation rows
+// and the partial records holds.  Measured on the sweep shape (K = 4096,
+// N = 14336) against the lanes-per-row kernel: M = 8 bf16 41.7 -> 21.7 us,
+// q8_0 43.0 -> 17.5, q4_0 34.5 -> 13.5; M = 4 q8_0 20.9 -> 16.7, q4_0
+// 19.9 -> 12.5, bf16 23.3 -> 21.2.  Eight warps with two slots each beat
+// sixteen warps in pairs sharing slots, and four.  Returns
+// BQG_ERR_UNSUPPORTED_SHAPE when it does not apply (the lanes-per-row plan
+// then serves the call).
+struct MmaPlan {
+    MmaParams p;
+    dim3 grid;
+    int threads;
+    size_t smem;
+};
+
+int plan_mma(int wf, int M, int64_t N, int64_t K, const DevInfo &dev, int device, MmaPlan *pl)
+{
+    static const bool off = env_int("BQG_NO_MMA", 0) != 0;
+    static const int force_D = env_int("BQG_MMA_D", 0);
+    static const int force_nw = env_int("BQG_MMA_WARPS", 0);
+    static const int force_gw = env_int("BQG_MMA_GROUP", 0);
+    if (off || (M != 4 && M != 8) || N <= 0) return BQG_ERR_UNSUPPORTED_SHAPE;
+    MmaParams p{};
+    p.N = N;
+    p.K = (int)K;
+    p.nb = (int)(K / QK);
+    const int slot = (wf == W_Q8_0) ? MmaGeom<W_Q8_0>::SLOT : (wf == W_Q4_0) ? MmaGeom<W_Q4_0>::SLOT
+                                                                              : MmaGeom<W_BF16>::SLOT;
+    p.T = (wf == W_BF16) ? (int)((K + 255) / 256) : (wf == W_Q4_0) ? (p.nb + 31) / 32 : (p.nb + 15) / 16;
+    p.units = (N + 15) / 16;
+    // bf16 weights over fewer units than half the SMs: the lanes-per-row
+    // kernel (split K) is faster (measured at N = 1024, M = 4 and 8)
+    if (wf == W_BF16 && p.units < dev.sms / 2) return BQG_ERR_UNSUPPORTED_SHAPE;
+    p.x_pitch = (int)((2 * K + 127) / 128 * 128 + 64);
+    const int xbytes = M * p.x_pitch;
+    if (xbytes > 80 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
+    p.gw = (force_gw == 1 || force_gw == 2) ? force_gw : 1;
+    p.nw = (force_nw >= 1 && force_nw <= 16) ? force_nw : 8;
+    p.nw = std::max(p.gw, p.nw / p.gw * p.gw);
+    const int ng = p.nw / p.gw;
+    const int ctas = (int)std::min<int64_t>(p.units, dev.sms);
+    const int64_t upc = (p.units + ctas - 1) / ctas;                 // units of the largest CTA
+    const int64_t maxS = upc * p.T;
+    if (maxS * ng >= ((int64_t)1 << 30) || upc * 16 * M >= ((int64_t)1 << 30)) return BQG_ERR_UNSUPPORTED_SHAPE;
+    const int64_t spg = (maxS + ng - 1) / ng;                        // stages of the busiest group
+    p.rmax = (int)std::max<int64_t>(1, std::min<int64_t>(upc, (spg + p.T - 2) / p.T + 1));
+    const int rec = p.nw * p.rmax * 512;
+    const int budget = 232448 - 512 - 128 - xbytes - rec - 8 * (ng * 4 + 1);
+    int D = std::min(4, budget / (ng * slot));
+    if (force_D > 0) D = std::min(D, force_D);
+    if (D < 1) return BQG_ERR_UNSUPPORTED_SHAPE;
+    p.D = D;
+    p.early = D;                                  // weights do not wait for the previous grid
+    p.x_off = ng * D * slot;
+    p.rec_off = p.x_off + xbytes;
+    p.bar_off = p.rec_off + rec;
+    MmaPlan g{};
+    g.smem = (size_t)p.bar_off + 8 * (ng * D + 1) + 128;      // + alignment slack
+    g.threads = 32 * p.nw;
+    g.grid = dim3((unsigned)ctas);
+    MmaFn fn = (wf == W_BF16) ? gemv_mma_run_bf16 : (wf == W_Q8_0) ? gemv_mma_run_q8_0 : gemv_mma_run_q4_0;
+    int bpsm = 0;
+    {
+        auto key = std::make_tuple(device, wf, (int)X_BF16, M, 0, g.threads, 2, g.smem);
+        std::unique_lock<std::mutex> lk(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) {
+            bpsm = it->second;
+        } else {
+            lk.unlock();
+            CUtensorMap dummy_map{};
+            const cudaError_t e = fn(dummy_map, dummy_map, p, M, dim3(1), g.threads, g.smem, 0, false, &bpsm);
+            if (e != cudaSuccess) return cuda_status(e);
+            lk.lock();
+            g_occ[key] = bpsm;
+        }
+    }
+    if (bpsm < 1) return BQG_ERR_UNSUPPORTED_SHAPE;
+    g.p = p;
+    *pl = g;
+    return BQG_OK;
+}
+
+int run_mma(int wf, int fmt, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    DevInfo dev;
+    int dv = 0;
+    int st = current_device(&dev);
+    if (st) return st;
+    cudaGetDevice(&dv);
+    MmaPlan g;
+    st = plan_mma(wf, M, N, K, dev, dv, &g);
+    if (st) return st;
+    auto enc = tensor_map_encoder();
+    if (!enc) return BQG_ERR_UNSUPPORTED_SHAPE;
+    // the repacked rows as 8-byte units; boxes of 16 rows: the stage's data
+    // plus the pitch pad (q8_0: a low or high code half; the scales)
+    const int64_t row_bytes = repacked_row_bytes(fmt, K);
+    const int box = (wf == W_Q8_0) ? MmaGeom<W_Q8_0>::BOX : (wf == W_Q4_0) ? MmaGeom<W_Q4_0>::BOX
+                                                                          : MmaGeom<W_BF16>::BOX;
+    cuuint64_t gdim[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)N};
+    cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t wbox[2] = {(cuuint32_t)box, 16u};
+    cuuint32_t sbox[2] = {(cuuint32_t)MmaGeom<W_Q8_0>::SC_BOX, 16u};
+    cuuint32_t estride[2] = {1u, 1u};
+    CUtensorMap wmap, smap;
+    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(Wp), gdim, gstride, wbox, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return BQG_ERR_UNSUPPORTED_SHAPE;
+    smap = wmap;
+    if (wf == W_Q8_0 &&
+        enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(Wp), gdim, gstride, sbox, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return BQG_ERR_UNSUPPORTED_SHAPE;
+    g.p.X = static_cast<const uint8_t *>(X);
+    g.p.Y = Y;
+    MmaFn fn = (wf == W_BF16) ? gemv_mma_run_bf16 : (wf == W_Q8_0) ? gemv_mma_run_q8_0 : gemv_mma_run_q4_0;
+    return cuda_status(fn(wmap, smap, g.p, M, g.grid, g.threads, g.smem, stream, g_pdl.load() != 0, nullptr));
+}
+
 int gemv_plain(int wf, int xf, int fmt, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
                void *ws, size_t ws_bytes, cudaStream_t stream)
 {
@@ -535,6 +668,10 @@ int gemv_plain(int wf, int xf, int fmt, const void *Wp, const void *X, float *Y,
     if (int st = check_k(K)) return st;
     if (wf == W_BF16 && K > 16384) return BQG_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(Wp) || !aligned16(Y) || !aligned(X, xf == X_Q8_1 ? 4 : 16)) return BQG_ERR_MISALIGNED;
+    if (xf == X_BF16 && (M == 4 || M == 8) && N > 0) {
+        const int st = run_mma(wf, fmt, Wp, X, Y, M, N, K, stream);
+        if (st != BQG_ERR_UNSUPPORTED_SHAPE) return st;
+    }
     GemvParams p{};
     p.W[0] = (const uint8_t *)Wp;
     p.Y[0] = Y;
@@ -913,10 +1050,52 @@ size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K)
     case BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1: Nv = 2 * N; unit = 2; break;
     default: return 0;
     }
+    if (op == BQG_OP_GEMV_BF16 || op == BQG_OP_GEMV_Q8_0 || op == BQG_OP_GEMV_Q4_0) {
+        MmaPlan mp;
+        if (plan_mma(wf, M, N, K, dev, dv, &mp) == BQG_OK) return 0;       // the tensor-core route
+    }
     GemvPlan g;
     if (plan_any(wf, xf, M, Nv, K, unit, dev, dv, &g) != BQG_OK) return 0;
     if (op == BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1 && g.splits == 1) return N % QK ? 0 : swiglu_q8_1_staging(M, N);
     return g.ws_bytes;
+}
+
+int bqg_gemv_route(int op, int M, int64_t N, int64_t K, int *route)
+{
+    if (!route || N <= 0 || !valid_m(M)) return BQG_ERR_INVALID_ARG;
+    if (int st = check_k(K)) return st;
+    int wf = W_Q4_0, xf = X_Q8_1;
+    switch (op) {
+    case BQG_OP_GEMV_BF16: wf = W_BF16; xf = X_BF16; break;
+    case BQG_OP_GEMV_Q8_0: wf = W_Q8_0; xf = X_BF16; break;
+    case BQG_OP_GEMV_Q4_0: wf = W_Q4_0; xf = X_BF16; break;
+    case BQG_OP_GEMV_Q4_0_Q8_1: break;
+    default: return BQG_ERR_INVALID_ARG;
+    }
+    if (wf == W_BF16 && K > 16384) return BQG_ERR_UNSUPPORTED_SHAPE;
+    DevInfo dev;
+    int dv = 0;
+    int st = current_device(&dev);
+    if (st) return st;
+    cudaGetDevice(&dv);
+    if (xf == X_BF16 && (M == 4 || M == 8)) {
+        MmaPlan mp;
+        st = plan_mma(wf, M, N, K, dev, dv, &mp);
+        if (st == BQG_OK) {
+            *route = BQG_ROUTE_TENSOR_CORE;
+            return BQG_OK;
+        }
+        if (st != BQG_ERR_UNSUPPORTED_SHAPE) return st;
+    }
+    GemvPlan g;
+    st = plan_any(wf, xf, M, N, K, 1, dev, dv, &g);
+    if (st) return st;
+    GemvParams p{};
+    p.nmat = 1;
+    p.epi = (g.splits > 1) ? EPI_PARTIAL : EPI_STORE;
+    *route = !g.lpr ? BQG_ROUTE_K_SLICE : rows_kernel_applies(g, p) ? BQG_ROUTE_LANES_PER_ROW_ROWS
+                                                                      : BQG_ROUTE_LANES_PER_ROW;
+    return BQG_OK;
 }
 
 int bqg_last_device_error(cudaStream_t stream, int *out)

@@ -562,23 +562,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_bf16_kernel(const __grid_
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+}  // namespace
+
+// cuTensorMapEncodeTiled from the driver, looked up once (thread-safe); null
+// when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
-
-}  // namespace
 
 int gemm_read_error(cudaStream_t stream, int *out)
 {
@@ -597,7 +597,7 @@ int gemm_bf16(int wf, const void *Wp, const void *X, float *Y, int M, int64_t N,
               int sms)
 {
     static std::mutex mu;
-    auto enc = encode_fn();
+    auto enc = tensor_map_encoder();
     if (!enc) return BQG_ERR_CUDA;
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};

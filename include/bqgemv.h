@@ -141,7 +141,16 @@ int bqg_rmsnorm_quantize_q8_1(const void *x, int x_dtype, const float *gamma, fl
  * ws/ws_bytes: workspace for split-K; bqg_workspace_size(op, M, N, K) bytes
  * are required when that size is non-zero (BQG_ERR_WORKSPACE otherwise); it
  * needs no initialisation and must not be shared by calls that overlap.
- * fp32 accumulation; bqg_gemv_q8_0/q4_0 dequantize (q*d, (q-8)*d) exactly.
+ * fp32 accumulation.  At M = 1 and 2 (and where the route below does not
+ * apply) bqg_gemv_q8_0/q4_0 dequantize (q*d, (q-8)*d) exactly and add the
+ * products in fp32.  At M = 4 and 8 (staged activations M*K*2 bytes within
+ * 80 KiB; bf16 weights with N >= 16 * 76) the products go to the tensor
+ * cores (mma.sync, bf16 operands: q8_0 codes, q4_0 values q-8 and bf16
+ * weights are exact in bf16, each product exact in fp32); each block's sum
+ * over its 32 values is then scaled by its d in fp32, and bf16 weights
+ * accumulate in the MMA's fp32 fragment.  Either way the result lies
+ * within 1e-3 * sum_k |w x| + 1e-6 of the exact sum (the bound the tests
+ * hold every route to).
  * Y may also be page-locked host memory given by its bqg_host_alias address
  * (the outputs are written there with plain stores over the CPU-GPU link);
  * this holds for the four bqg_gemv_* entries of a single matrix and
@@ -300,6 +309,19 @@ int bqg_debug_q4_0_q8_1_block_dots_kslice(const void *Wp, const void *Xq, int32_
 /* Workspace bytes that op needs for this shape on the current device
  * (0 = none).  For BQG_OP_QKV_Q4_0_Q8_1 pass N = Nq + 2*Nkv. */
 size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K);
+
+/* Which kernel serves a GEMV call of this shape on the current device
+ * (op: BQG_OP_GEMV_BF16, _Q8_0, _Q4_0 or _Q4_0_Q8_1): *route receives one
+ * of the BQG_ROUTE_* values below.  No launch; the choice depends only on
+ * the shape, the device and the BQG_* tuning variables.  Errors as the
+ * GEMV entry points' shape checks. */
+enum {
+    BQG_ROUTE_K_SLICE = 0,                /* K-slice kernel (staged activations too large) */
+    BQG_ROUTE_LANES_PER_ROW = 1,          /* lanes-per-row kernel, general form (split K) */
+    BQG_ROUTE_LANES_PER_ROW_ROWS = 2,     /* lanes-per-row kernel, whole rows per stage */
+    BQG_ROUTE_TENSOR_CORE = 3             /* tensor-core kernel (M = 4, 8; bf16 activations) */
+};
+int bqg_gemv_route(int op, int M, int64_t N, int64_t K, int *route);
 
 /* Reads and clears this device's error word, which a bounded device-side
  * wait sets when it gives up (0 = none).  Synchronizes `stream` first.

@@ -212,6 +212,40 @@ def test_gemv_q4_0_q8_1(ora, M, N, K):
     run_gemv(ora, Q4_0, Q8_1, M, N, K, seed=N + K + M)
 
 
+OPS = {BF16: bqg.OP_GEMV_BF16, Q8_0: bqg.OP_GEMV_Q8_0, Q4_0: bqg.OP_GEMV_Q4_0}
+# Shapes the tensor-core kernel serves at M = 4 and 8: N not a multiple of
+# its 16-row units (17, 1300, 2437) and K whose last stage is partial (K =
+# 1056: one block past a q4_0 tile, one past a q8_0 half tile, 32 values
+# past a bf16 tile; K = 4128 likewise after four tiles).  bf16 weights take
+# the route from N = 16 * 76 rows on.
+TC_SHAPES = [(17, 1056), (1300, 4128), (2437, 1056), (2437, 4096)]
+
+
+@pytest.mark.parametrize("M", [4, 8])
+@pytest.mark.parametrize("fmt", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("N,K", TC_SHAPES)
+def test_gemv_tensor_core_route(ora, fmt, M, N, K):
+    route = bqg.gemv_route(OPS[fmt], M, N, K)
+    want_tc = not (fmt == BF16 and N < 16 * 76)
+    assert (route == bqg.ROUTE_TENSOR_CORE) == want_tc, bqg.ROUTE_NAMES[route]
+    run_gemv(ora, fmt, BF16, M, N, K, seed=3 * N + K + M)
+
+
+def test_gemv_routes():
+    """The route each shape class takes (no launch)."""
+    tc, rows = bqg.ROUTE_TENSOR_CORE, bqg.ROUTE_LANES_PER_ROW_ROWS
+    assert bqg.gemv_route(bqg.OP_GEMV_Q8_0, 8, 14336, 4096) == tc
+    assert bqg.gemv_route(bqg.OP_GEMV_BF16, 4, 14336, 4096) == tc
+    assert bqg.gemv_route(bqg.OP_GEMV_Q4_0, 4, 14336, 4096) == tc
+    # M = 1: the whole-row lanes-per-row kernel on the headline shape
+    assert bqg.gemv_route(bqg.OP_GEMV_BF16, 1, 12288, 4096) == rows
+    assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, 1, 12288, 4096) == rows
+    # q8_1 activations never take the tensor-core route
+    assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, 8, 14336, 4096) != tc
+    # staged activations above 80 KiB (M = 8, K = 11008): not the tensor-core route
+    assert bqg.gemv_route(bqg.OP_GEMV_Q8_0, 8, 4096, 11008) != tc
+
+
 @pytest.mark.parametrize("N,K", [(64, 1024), (1000, 4096), (130, 11008)])
 def test_gemv_q4_0_q8_1_float_is_the_exact_integer_dots_scaled(ora, N, K):
     """Each output is sum_b fp32(d_w d_x) * sumi_b with sumi_b the exact
