@@ -586,17 +586,21 @@ int plan_mma(int wf, int M, int64_t N, int64_t K, const DevInfo &dev, int device
     const int64_t spg = (maxS + ng - 1) / ng;                        // stages of the busiest group
     p.rmax = (int)std::max<int64_t>(1, std::min<int64_t>(upc, (spg + p.T - 2) / p.T + 1));
     const int rec = p.nw * p.rmax * 512;
-    const int budget = 232448 - 512 - 128 - xbytes - rec - 8 * (ng * 4 + 1);
+    const int64_t xarea = std::max<int64_t>(xbytes, (int64_t)M * (16 * upc + 1) * 4 + 15) / 16 * 16;
+    if (xarea > 120 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
+    const int budget = 232448 - 512 - 128 - (int)xarea - rec - 8 * ng * 4;
     int D = std::min(4, budget / (ng * slot));
     if (force_D > 0) D = std::min(D, force_D);
     if (D < 1) return BQG_ERR_UNSUPPORTED_SHAPE;
     p.D = D;
-    p.early = D;                                  // weights do not wait for the previous grid
+    static const int force_early = env_int("BQG_MMA_EARLY", -1);
+    p.early = (force_early >= 0) ? std::min(force_early, D) : D;   // weights do not wait for the previous grid
     p.x_off = ng * D * slot;
-    p.rec_off = p.x_off + xbytes;
+    // the activation area also holds the CTA's sums before they go out
+    p.rec_off = p.x_off + (int)xarea;
     p.bar_off = p.rec_off + rec;
     MmaPlan g{};
-    g.smem = (size_t)p.bar_off + 8 * (ng * D + 1) + 128;      // + alignment slack
+    g.smem = (size_t)p.bar_off + 8 * ng * D + 128;      // + alignment slack
     g.threads = 32 * p.nw;
     g.grid = dim3((unsigned)ctas);
     MmaFn fn = (wf == W_BF16) ? gemv_mma_run_bf16 : (wf == W_Q8_0) ? gemv_mma_run_q8_0 : gemv_mma_run_q4_0;

@@ -139,13 +139,6 @@ __device__ __forceinline__ float scale_of(const uint4 &s, int i)
     return half_bits_to_float((i & 1) ? (w >> 16) : (w & 0xffffu));
 }
 
-// The partial record of one unit: lane l's four sums (rows g, g + 8 x
-// activation columns 2t, 2t + 1) at floats 4l .. 4l + 3.
-__device__ __forceinline__ int mma_record_index(int r, int m)
-{
-    return ((r & 7) * 4 + (m >> 1)) * 4 + (r >> 3) * 2 + (m & 1);
-}
-
 // One block of 32 values (bf16: two 16-value chunks) of the lane's weight
 // rows g and g + 8 against its 16 activation bytes xq, added into cb (for
 // q8_0 / q4_0 a fresh fragment, scaled afterwards).  st: the slot; s: the
@@ -220,7 +213,6 @@ __global__ void __launch_bounds__(512, 1)
     const int nbx = p.K / 32;                      // blocks of 32 values per row
     const uint32_t bar0 = smem_u32(smem + p.bar_off);
     const uint32_t wbar = bar0 + 8 * grp * D;
-    const uint32_t xbar = bar0 + 8 * NG * D;
     const uint32_t slot0 = smem_u32(smem) + (uint32_t)(grp * D * G::SLOT);
     uint8_t *xs = smem + p.x_off;
     float *rec = reinterpret_cast<float *>(smem + p.rec_off);
@@ -260,9 +252,17 @@ __global__ void __launch_bounds__(512, 1)
         return r != 0;
     };
 
+    // the activation rows: into L2 first (ahead of the weight copies in the
+    // SM's copy queue; each CTA its 1/grid share), into shared memory once
+    // the previous grid has completed (it may be their producer)
+    if (tid == 32) {
+        const uint32_t xb = (uint32_t)(M * p.K * 2);
+        const uint32_t ch = ((xb + gridDim.x - 1) / gridDim.x + 15) & ~15u;
+        const uint32_t at = blockIdx.x * ch;
+        if (at < xb) prefetch_l2_bulk(p.X + at, min(ch, xb - at));
+    }
     if (tid == 0) {
         for (int i = 0; i < NG * D; i++) mbar_init(bar0 + 8 * i, 1);
-        mbar_init(xbar, 1);
         s_abort = 0;
         mbar_fence_init();
     }
@@ -275,33 +275,46 @@ __global__ void __launch_bounds__(512, 1)
     const int first = min(D, nst);
     if (leader)
         for (; issued < min(first, p.early); issued++) issue(issued, issued);
-    // the activation rows: into L2 now, into shared memory once the
-    // previous grid has completed (it may be their producer)
-    if (tid == 32) prefetch_l2_bulk(p.X, (uint32_t)(M * p.K * 2));
     pdl_wait();
     pdl_launch_dependents();
-    if (tid == 0) {
-        mbar_arrive_expect_tx(xbar, (uint32_t)(M * p.K * 2));
-        for (int m = 0; m < M; m++)
-            bulk_g2s(smem_u32(xs + m * p.x_pitch), p.X + (size_t)m * p.K * 2, (uint32_t)p.K * 2, xbar);
-    }
     if (leader)
         for (; issued < first; issued++) issue(issued, issued);
-    const bool xok = mbar_wait_bounded(xbar, 0);
-    if (!xok) {
-        atomicExch(&g_gemv_error, 1);
-        s_abort = 1;
-    }
-    // permuted in place: of each 32 values, lane t's 16 bytes (values
-    // 4t .. 4t + 3 and 16 + 4t .. 16 + 4t + 3) at 16 t
-    for (int i = xok ? tid : M * nbx; i < M * nbx; i += blockDim.x) {
-        const int m = i / nbx, b = i - m * nbx;
-        uint4 *blk = reinterpret_cast<uint4 *>(xs + m * p.x_pitch + b * 64);
-        const uint4 v0 = blk[0], v1 = blk[1], v2 = blk[2], v3 = blk[3];
-        blk[0] = make_uint4(v0.x, v0.y, v2.x, v2.y);
-        blk[1] = make_uint4(v0.z, v0.w, v2.z, v2.w);
-        blk[2] = make_uint4(v1.x, v1.y, v3.x, v3.y);
-        blk[3] = make_uint4(v1.z, v1.w, v3.z, v3.w);
+    // The activation rows by plain loads (they would queue behind the weight
+    // copies in the tensor-copy unit), all of a thread's loads in flight at
+    // once, permuted on the way in: of each 32 values, lane t's 16 bytes
+    // (values 4t .. 4t + 3 and 16 + 4t .. 16 + 4t + 3) at 16 t.
+    {
+        // every CTA reads all of X: each starts at its own offset, so that at
+        // any moment the CTAs ask different L2 lines for it
+        constexpr int XU = 4;                      // blocks of 64 B per thread and round
+        const int nblk = M * nbx;
+        const int rot = (int)(((int64_t)blockIdx.x * 97) % nblk);
+        for (int i0 = tid; i0 < nblk; i0 += XU * (int)blockDim.x) {
+            uint4 v[XU][4];
+#pragma unroll
+            for (int k = 0; k < XU; k++) {
+                int i = i0 + k * (int)blockDim.x + rot;
+                i -= (i >= nblk) ? nblk : 0;
+                if (i0 + k * (int)blockDim.x < nblk) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.X) + (size_t)i * 4;   // rows are contiguous
+#pragma unroll
+                    for (int c = 0; c < 4; c++) v[k][c] = src[c];
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < XU; k++) {
+                int i = i0 + k * (int)blockDim.x + rot;
+                i -= (i >= nblk) ? nblk : 0;
+                if (i0 + k * (int)blockDim.x < nblk) {
+                    const int m = i / nbx, b = i - m * nbx;
+                    uint4 *blk = reinterpret_cast<uint4 *>(xs + m * p.x_pitch + b * 64);
+                    blk[0] = make_uint4(v[k][0].x, v[k][0].y, v[k][2].x, v[k][2].y);
+                    blk[1] = make_uint4(v[k][0].z, v[k][0].w, v[k][2].z, v[k][2].w);
+                    blk[2] = make_uint4(v[k][1].x, v[k][1].y, v[k][3].x, v[k][3].y);
+                    blk[3] = make_uint4(v[k][1].z, v[k][1].w, v[k][3].z, v[k][3].w);
+                }
+            }
+        }
     }
     __syncthreads();
 
@@ -363,7 +376,9 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (++d == D) { d = 0; ph ^= 1; }
         if (ts == T - 1 || q == nst - 1) {
-            // this warp's part of unit ul: a record of 128 floats
+            // this warp's part of unit ul: a record of 128 floats, lane l's
+            // four sums (rows g, g + 8 x activation columns 2t, 2t + 1) at
+            // floats 4l .. 4l + 3
             reinterpret_cast<float4 *>(rec + (warp * p.rmax + ul - ul_first) * 128)[lane] =
                 make_float4(c[0], c[1], c[2], c[3]);
             c[0] = c[1] = c[2] = c[3] = 0.f;
@@ -374,27 +389,44 @@ __global__ void __launch_bounds__(512, 1)
         for (int q = waited; q < issued; q++)
             mbar_wait_bounded(wbar + 8 * (q % D), (uint32_t)((q / D) & 1));
     }
-    if (tid == 0 && !xok) mbar_wait_bounded(xbar, 0);
     __syncthreads();
     if (*(volatile int *)&s_abort) return;
 
-    // Y[m, 16 (u0 + ul) + r]: the unit's records added in warp order
+    // Y[m, 16 (u0 + ul) + r]: the unit's records added in warp order.  Thread
+    // o takes float o & 127 of unit o >> 7's records (consecutive words: no
+    // bank conflicts) and parks the sum in the staged-activation area, from
+    // where the rows of Y go out contiguous.
     const int U = (int)(u1 - u0);
-    const int outs = U * 16 * M;
-    for (int o = tid; o < outs; o += blockDim.x) {
-        const int m = o / (U * 16);
-        const int rr = o - m * U * 16;
-        const int ul = rr >> 4;
-        const int r = rr & 15;
-        const int64_t row = (u0 + ul) * 16 + r;
-        if (row >= p.N) continue;
-        const int idx = mma_record_index(r, m);
+    const int ypitch = U * 16 + 1;
+    float *ys = reinterpret_cast<float *>(xs);     // M x ypitch floats (the activations are done)
+    int wf[16], wl[16];                            // the warps' unit ranges, in registers
+#pragma unroll
+    for (int w = 0; w < 16; w++) {
+        wf[w] = (w < NW) ? s_first[w] : 1;
+        wl[w] = (w < NW) ? s_last[w] : 0;
+    }
+    for (int o = tid; o < U * 128; o += blockDim.x) {
+        const int ul = o >> 7, idx = o & 127;
+        const int l = idx >> 2, reg = idx & 3;     // the record's lane and register
+        const int m = ((l & 3) << 1) | (reg & 1);
+        const int r = (l >> 2) | ((reg >> 1) << 3);
+        if (m >= M) continue;
+        float part[16];
+#pragma unroll
+        for (int w = 0; w < 16; w++)               // independent loads, then the sum in warp order
+            part[w] = (ul >= wf[w] && ul <= wl[w]) ? rec[(w * p.rmax + ul - wf[w]) * 128 + idx] : 0.f;
         float sum = 0.f;
-        for (int w = 0; w < NW; w++) {
-            const int f = s_first[w];
-            if (ul >= f && ul <= s_last[w]) sum += rec[(w * p.rmax + ul - f) * 128 + idx];
-        }
-        p.Y[(int64_t)m * p.N + row] = sum;
+#pragma unroll
+        for (int w = 0; w < 16; w++)
+            if (ul >= wf[w] && ul <= wl[w]) sum += part[w];
+        ys[m * ypitch + ul * 16 + r] = sum;
+    }
+    __syncthreads();
+    const int64_t row0 = u0 * 16;
+    const int nr = (int)(min(u1 * 16, p.N) - row0);
+    for (int o = tid; o < M * nr; o += blockDim.x) {
+        const int m = o / nr, r = o - m * nr;
+        p.Y[(int64_t)m * p.N + row0 + r] = ys[m * ypitch + r];
     }
 }
 
