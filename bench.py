@@ -668,8 +668,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--json-out", default=None)
     ap.add_argument("--min-warm-s", type=float, default=1.0, help="minimum warm-up time per arm")
-    ap.add_argument("--profile", default=None, choices=["bf16", "q8_0", "q4_0", "q4_0_q8_1", "gemm"],
-                    help="profiling case: only this M=1 K=4096 N=12288 arm, 2 weight sets, eager calls")
+    ap.add_argument("--profile", default=None,
+                    help="profiling case, 2 weight sets, eager calls: gemm, or a GEMV arm bf16 | q8_0 | "
+                         "q4_0 | q4_0_q8_1 (M=1 K=4096 N=12288), optionally ':<N>x<M>' (K=4096)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -727,10 +728,13 @@ def main():
         print(json.dumps({"profile": arm.name, "calls": args.warmup + args.steps}))
         return 0
     if args.profile:
-        # a small case for ncu: two weight sets (cache state is ncu's to control)
-        fmt = {"bf16": bqg.BF16, "q8_0": bqg.Q8_0, "q4_0": bqg.Q4_0, "q4_0_q8_1": bqg.Q4_0}[args.profile]
-        xf = bqg.Q8_1 if args.profile == "q4_0_q8_1" else bqg.BF16
-        arm = GemvArm(fmt, xf, 1, N_HEAD, K_HEAD, sets=2)
+        # a small case for ncu: two weight sets (cache state is ncu's to control);
+        # "<fmt>" is the headline shape, "<fmt>:<N>x<M>" another (K = 4096)
+        name, shape = (args.profile.split(":") + [f"{N_HEAD}x1"])[:2]
+        n_rows, m_rows = map(int, shape.split("x"))
+        fmt = {"bf16": bqg.BF16, "q8_0": bqg.Q8_0, "q4_0": bqg.Q4_0, "q4_0_q8_1": bqg.Q4_0}[name]
+        xf = bqg.Q8_1 if name == "q4_0_q8_1" else bqg.BF16
+        arm = GemvArm(fmt, xf, m_rows, n_rows, K_HEAD, sets=2)
         for i in range(args.warmup + args.steps):
             arm.call(i)
         torch.cuda.synchronize()
