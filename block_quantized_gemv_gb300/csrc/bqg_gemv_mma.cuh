@@ -282,36 +282,37 @@ __global__ void __launch_bounds__(512, 1)
     // The activation rows by plain loads (they would queue behind the weight
     // copies in the tensor-copy unit), all of a thread's loads in flight at
     // once, permuted on the way in: of each 32 values, lane t's 16 bytes
-    // (values 4t .. 4t + 3 and 16 + 4t .. 16 + 4t + 3) at 16 t.
+    // (values 4t .. 4t + 3 and 16 + 4t .. 16 + 4t + 3) at 16 t.  Thread i
+    // writes staged chunk i (consecutive threads, consecutive chunks: no
+    // bank conflicts) from its two 8-byte source pieces.  Every CTA reads all
+    // of X: each starts at its own offset, so that at any moment the CTAs
+    // ask different L2 lines for it.
     {
-        // every CTA reads all of X: each starts at its own offset, so that at
-        // any moment the CTAs ask different L2 lines for it
-        constexpr int XU = 4;                      // blocks of 64 B per thread and round
-        const int nblk = M * nbx;
-        const int rot = (int)(((int64_t)blockIdx.x * 97) % nblk);
-        for (int i0 = tid; i0 < nblk; i0 += XU * (int)blockDim.x) {
-            uint4 v[XU][4];
+        constexpr int XU = 8;                      // chunks per thread and round
+        const int n16 = M * nbx * 4;
+        const int rot = (int)(((int64_t)blockIdx.x * 389) % n16);
+        const uint2 *src = reinterpret_cast<const uint2 *>(p.X);
+        for (int i0 = tid; i0 < n16; i0 += XU * (int)blockDim.x) {
+            uint2 lo[XU], hi[XU];
 #pragma unroll
             for (int k = 0; k < XU; k++) {
                 int i = i0 + k * (int)blockDim.x + rot;
-                i -= (i >= nblk) ? nblk : 0;
-                if (i0 + k * (int)blockDim.x < nblk) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(p.X) + (size_t)i * 4;   // rows are contiguous
-#pragma unroll
-                    for (int c = 0; c < 4; c++) v[k][c] = src[c];
+                i -= (i >= n16) ? n16 : 0;
+                if (i0 + k * (int)blockDim.x < n16) {
+                    const int blk = i >> 2, c = i & 3;          // rows are contiguous: block blk of X
+                    lo[k] = src[(size_t)blk * 8 + c];
+                    hi[k] = src[(size_t)blk * 8 + 4 + c];
                 }
             }
 #pragma unroll
             for (int k = 0; k < XU; k++) {
                 int i = i0 + k * (int)blockDim.x + rot;
-                i -= (i >= nblk) ? nblk : 0;
-                if (i0 + k * (int)blockDim.x < nblk) {
-                    const int m = i / nbx, b = i - m * nbx;
-                    uint4 *blk = reinterpret_cast<uint4 *>(xs + m * p.x_pitch + b * 64);
-                    blk[0] = make_uint4(v[k][0].x, v[k][0].y, v[k][2].x, v[k][2].y);
-                    blk[1] = make_uint4(v[k][0].z, v[k][0].w, v[k][2].z, v[k][2].w);
-                    blk[2] = make_uint4(v[k][1].x, v[k][1].y, v[k][3].x, v[k][3].y);
-                    blk[3] = make_uint4(v[k][1].z, v[k][1].w, v[k][3].z, v[k][3].w);
+                i -= (i >= n16) ? n16 : 0;
+                if (i0 + k * (int)blockDim.x < n16) {
+                    const int blk = i >> 2, c = i & 3;
+                    const int m = blk / nbx, b = blk - m * nbx;
+                    *reinterpret_cast<uint4 *>(xs + m * p.x_pitch + b * 64 + 16 * c) =
+                        make_uint4(lo[k].x, lo[k].y, hi[k].x, hi[k].y);
                 }
             }
         }
