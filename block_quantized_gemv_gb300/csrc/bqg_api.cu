@@ -362,7 +362,9 @@ int plan_lpr(int wf, int xf, int M, int64_t Nv, int64_t K, int unit, const DevIn
     g.stride = (int)range_bytes(wf, std::min(g.piece_chunks, g.cps));
     const int64_t stage = (int64_t)g.S * g.stride;
     if (budget < stage) return BQG_ERR_UNSUPPORTED_SHAPE;
-    const int max_warps = (overlap || M >= 4) ? 8 : kLprMaxWarps;   // M >= 4: the kernel's 256-thread bound
+    static const int force_warps = env_int("BQG_LPR_WARPS", 0);
+    int max_warps = (overlap || M >= 4) ? 8 : kLprMaxWarps;         // M >= 4: the kernel's 256-thread bound
+    if (force_warps >= 1) max_warps = std::min(max_warps, force_warps);
     const int slots = (int)std::min<int64_t>(64, budget / stage);
     int ng = std::max(1, std::min(max_warps, slots / 2));
     int D = std::max(1, slots / ng);
