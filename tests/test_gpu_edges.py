@@ -65,10 +65,13 @@ def degenerate_canonical(fmt, N, K, seed):
     return canon.reshape(N, nb * bb)
 
 
-@pytest.mark.parametrize("M", [2, 8])
+@pytest.mark.parametrize("M", [2, 4, 8])
 @pytest.mark.parametrize("fmt,xf", [(Q8_0, BF16), (Q4_0, BF16), (Q4_0, Q8_1)])
 def test_gemv_degenerate_blocks_and_a_zero_row(ora, fmt, xf, M):
     N, K = 64, 4096
+    if xf == BF16 and M >= 4:      # these calls take the tensor-core route
+        op = bqg.OP_GEMV_Q8_0 if fmt == Q8_0 else bqg.OP_GEMV_Q4_0
+        assert bqg.gemv_route(op, M, N, K) == bqg.ROUTE_TENSOR_CORE
     canon = degenerate_canonical(fmt, N, K, seed=M + fmt)
     Wp = gpu_repacked(fmt, canon, N, K)
     x = synth.activations_f32(M, K, seed=77)
@@ -106,3 +109,25 @@ def test_tensor_on_another_device_is_refused_before_launch(monkeypatch):
     monkeypatch.undo()
     torch.cuda.synchronize()
     assert torch.all(Y == 7.0)          # nothing ran
+
+
+@pytest.mark.parametrize("fmt", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("K,tensor_core", [(5056, True), (5088, False)])
+def test_tensor_core_route_at_its_largest_k(ora, fmt, K, tensor_core):
+    """At M = 8 the tensor-core route stages the activation rows at a pitch of
+    round_up(2K, 128) + 64 bytes within 80 KiB: K = 5056 is the largest that
+    fits, K = 5088 goes to the lanes-per-row kernel.  Both match the oracle."""
+    M, N = 8, 2437
+    op = {BF16: bqg.OP_GEMV_BF16, Q8_0: bqg.OP_GEMV_Q8_0, Q4_0: bqg.OP_GEMV_Q4_0}[fmt]
+    assert (bqg.gemv_route(op, M, N, K) == bqg.ROUTE_TENSOR_CORE) == tensor_core
+    Wf = synth.weights_f32(N, K, seed=K + fmt)
+    canon = synth.bf16_bits(Wf) if fmt == BF16 else ora.quantize(fmt, Wf)
+    Wp = gpu_repacked(fmt, canon, N, K)
+    xref = synth.bf16_bits(synth.activations_f32(M, K, seed=K + 1))
+    Y = nan_like((M, N))
+    fn = {BF16: bqg.gemv_bf16, Q8_0: bqg.gemv_q8_0, Q4_0: bqg.gemv_q4_0}[fmt]
+    fn(Wp, synth.bf16_tensor(xref), N, K, out=Y, ws=bqg.workspace(op, M, N, K))
+    torch.cuda.synchronize()
+    Yr, Ar = ora.gemv(fmt, canon, BF16, xref, M, N, K, nthreads=8)
+    check_close(Y, Yr, Ar, f"fmt {fmt} M=8 K={K}")
+
