@@ -32,6 +32,7 @@ using MmaFn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const Mm
 cudaError_t gemv_mma_run_bf16(const CUtensorMap &, const CUtensorMap &, const MmaParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_mma_run_q8_0(const CUtensorMap &, const CUtensorMap &, const MmaParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 cudaError_t gemv_mma_run_q4_0(const CUtensorMap &, const CUtensorMap &, const MmaParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
+cudaError_t gemv_mma_run_q4_0_q8_1(const CUtensorMap &, const CUtensorMap &, const MmaParams &, int, dim3, int, size_t, cudaStream_t, bool, int *);
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 int gemv_x_stage_bytes_bf16(int, int, int);
 int gemv_x_stage_bytes_q8_0(int, int, int);
@@ -556,13 +557,22 @@ struct MmaPlan {
     size_t smem;
 };
 
-int plan_mma(int wf, int M, int64_t N, int64_t K, const DevInfo &dev, int device, MmaPlan *pl)
+MmaFn mma_runner(int wf, int xf)
+{
+    if (xf == X_Q8_1) return gemv_mma_run_q4_0_q8_1;
+    return (wf == W_BF16) ? gemv_mma_run_bf16 : (wf == W_Q8_0) ? gemv_mma_run_q8_0 : gemv_mma_run_q4_0;
+}
+
+int plan_mma(int wf, int xf, int M, int64_t N, int64_t K, const DevInfo &dev, int device, MmaPlan *pl)
 {
     static const bool off = env_int("BQG_NO_MMA", 0) != 0;
     static const int force_D = env_int("BQG_MMA_D", 0);
     static const int force_nw = env_int("BQG_MMA_WARPS", 0);
     static const int force_gw = env_int("BQG_MMA_GROUP", 0);
     if (off || (M != 4 && M != 8) || N <= 0) return BQG_ERR_UNSUPPORTED_SHAPE;
+    // q8_1 activations (q4_0 weights): at M = 8, where the integer-dot
+    // lanes-per-row kernel is bound by its dots (at M = 4 it is faster)
+    if (xf == X_Q8_1 && (wf != W_Q4_0 || M != 8)) return BQG_ERR_UNSUPPORTED_SHAPE;
     MmaParams p{};
     p.N = N;
     p.K = (int)K;
@@ -575,8 +585,9 @@ int plan_mma(int wf, int M, int64_t N, int64_t K, const DevInfo &dev, int device
     // kernel (split K) is faster (measured at N = 1024, M = 4 and 8)
     if (wf == W_BF16 && p.units < dev.sms / 2) return BQG_ERR_UNSUPPORTED_SHAPE;
     p.x_pitch = (int)((2 * K + 127) / 128 * 128 + 64);
-    const int xbytes = M * p.x_pitch;
-    if (xbytes > 80 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
+    const int xdbytes = (xf == X_Q8_1) ? p.nb * 8 * 4 : 0;              // q8_1: the scale table
+    const int xbytes = M * p.x_pitch + xdbytes;
+    if (M * p.x_pitch > 80 * 1024) return BQG_ERR_UNSUPPORTED_SHAPE;
     p.gw = (force_gw == 1 || force_gw == 2) ? force_gw : 1;
     p.nw = (force_nw >= 1 && force_nw <= 16) ? force_nw : 8;
     p.nw = std::max(p.gw, p.nw / p.gw * p.gw);
@@ -598,6 +609,7 @@ int plan_mma(int wf, int M, int64_t N, int64_t K, const DevInfo &dev, int device
     static const int force_early = env_int("BQG_MMA_EARLY", -1);
     p.early = (force_early >= 0) ? std::min(force_early, D) : D;   // weights do not wait for the previous grid
     p.x_off = ng * D * slot;
+    p.xd_off = p.x_off + M * p.x_pitch;
     // the activation area also holds the CTA's sums before they go out
     p.rec_off = p.x_off + (int)xarea;
     p.bar_off = p.rec_off + rec;
@@ -605,10 +617,10 @@ int plan_mma(int wf, int M, int64_t N, int64_t K, const DevInfo &dev, int device
     g.smem = (size_t)p.bar_off + 8 * ng * D + 128;      // + alignment slack
     g.threads = 32 * p.nw;
     g.grid = dim3((unsigned)ctas);
-    MmaFn fn = (wf == W_BF16) ? gemv_mma_run_bf16 : (wf == W_Q8_0) ? gemv_mma_run_q8_0 : gemv_mma_run_q4_0;
+    MmaFn fn = mma_runner(wf, xf);
     int bpsm = 0;
     {
-        auto key = std::make_tuple(device, wf, (int)X_BF16, M, 0, g.threads, 2, g.smem);
+        auto key = std::make_tuple(device, wf, xf, M, 0, g.threads, 2, g.smem);
         std::unique_lock<std::mutex> lk(g_mu);
         auto it = g_occ.find(key);
         if (it != g_occ.end()) {
@@ -628,7 +640,8 @@ int plan_mma(int wf, int M, int64_t N, int64_t K, const DevInfo &dev, int device
     return BQG_OK;
 }
 
-int run_mma(int wf, int fmt, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K, cudaStream_t stream)
+int run_mma(int wf, int xf, int fmt, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
+            cudaStream_t stream)
 {
     DevInfo dev;
     int dv = 0;
@@ -636,7 +649,7 @@ int run_mma(int wf, int fmt, const void *Wp, const void *X, float *Y, int M, int
     if (st) return st;
     cudaGetDevice(&dv);
     MmaPlan g;
-    st = plan_mma(wf, M, N, K, dev, dv, &g);
+    st = plan_mma(wf, xf, M, N, K, dev, dv, &g);
     if (st) return st;
     auto enc = tensor_map_encoder();
     if (!enc) return BQG_ERR_UNSUPPORTED_SHAPE;
@@ -663,8 +676,8 @@ int run_mma(int wf, int fmt, const void *Wp, const void *X, float *Y, int M, int
         return BQG_ERR_UNSUPPORTED_SHAPE;
     g.p.X = static_cast<const uint8_t *>(X);
     g.p.Y = Y;
-    MmaFn fn = (wf == W_BF16) ? gemv_mma_run_bf16 : (wf == W_Q8_0) ? gemv_mma_run_q8_0 : gemv_mma_run_q4_0;
-    return cuda_status(fn(wmap, smap, g.p, M, g.grid, g.threads, g.smem, stream, g_pdl.load() != 0, nullptr));
+    return cuda_status(mma_runner(wf, xf)(wmap, smap, g.p, M, g.grid, g.threads, g.smem, stream, g_pdl.load() != 0,
+                                          nullptr));
 }
 
 int gemv_plain(int wf, int xf, int fmt, const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
@@ -674,8 +687,8 @@ int gemv_plain(int wf, int xf, int fmt, const void *Wp, const void *X, float *Y,
     if (int st = check_k(K)) return st;
     if (wf == W_BF16 && K > 16384) return BQG_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(Wp) || !aligned16(Y) || !aligned(X, xf == X_Q8_1 ? 4 : 16)) return BQG_ERR_MISALIGNED;
-    if (xf == X_BF16 && (M == 4 || M == 8) && N > 0) {
-        const int st = run_mma(wf, fmt, Wp, X, Y, M, N, K, stream);
+    if ((M == 4 || M == 8) && N > 0) {
+        const int st = run_mma(wf, xf, fmt, Wp, X, Y, M, N, K, stream);
         if (st != BQG_ERR_UNSUPPORTED_SHAPE) return st;
     }
     GemvParams p{};
@@ -1056,9 +1069,9 @@ size_t bqg_workspace_size(int op, int M, int64_t N, int64_t K)
     case BQG_OP_GATE_UP_Q8_1_Q4_0_Q8_1: Nv = 2 * N; unit = 2; break;
     default: return 0;
     }
-    if (op == BQG_OP_GEMV_BF16 || op == BQG_OP_GEMV_Q8_0 || op == BQG_OP_GEMV_Q4_0) {
+    if (op == BQG_OP_GEMV_BF16 || op == BQG_OP_GEMV_Q8_0 || op == BQG_OP_GEMV_Q4_0 || op == BQG_OP_GEMV_Q4_0_Q8_1) {
         MmaPlan mp;
-        if (plan_mma(wf, M, N, K, dev, dv, &mp) == BQG_OK) return 0;       // the tensor-core route
+        if (plan_mma(wf, xf, M, N, K, dev, dv, &mp) == BQG_OK) return 0;   // the tensor-core route
     }
     GemvPlan g;
     if (plan_any(wf, xf, M, Nv, K, unit, dev, dv, &g) != BQG_OK) return 0;
@@ -1084,9 +1097,9 @@ int bqg_gemv_route(int op, int M, int64_t N, int64_t K, int *route)
     int st = current_device(&dev);
     if (st) return st;
     cudaGetDevice(&dv);
-    if (xf == X_BF16 && (M == 4 || M == 8)) {
+    if (M == 4 || M == 8) {
         MmaPlan mp;
-        st = plan_mma(wf, M, N, K, dev, dv, &mp);
+        st = plan_mma(wf, xf, M, N, K, dev, dv, &mp);
         if (st == BQG_OK) {
             *route = BQG_ROUTE_TENSOR_CORE;
             return BQG_OK;

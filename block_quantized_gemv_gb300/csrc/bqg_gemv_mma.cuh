@@ -44,7 +44,7 @@
 namespace bqg {
 
 struct MmaParams {
-    const uint8_t *X;       // bf16 [M][K]
+    const uint8_t *X;       // bf16 [M][K], or q8_1 blocks [M][K/32] (q4_0 weights)
     float *Y;               // [M][N]
     int64_t N;              // weight rows
     int K;
@@ -58,6 +58,7 @@ struct MmaParams {
     int rmax;               // partial records per warp
     int x_pitch;            // staged activation row pitch: round_up(2K, 128) + 64
     int x_off, rec_off, bar_off;  // shared-memory offsets
+    int xd_off;             // q8_1 activations: their block scales d, [K/32][8] floats
 };
 
 // Stage geometry per weight format: row pitch in the slot, blocks of 32
@@ -132,6 +133,18 @@ __device__ __forceinline__ void q4_word_bf16(uint32_t w, uint32_t &l01, uint32_t
     asm("sub.rn.bf16x2 %0, %0, %1;" : "+r"(h23) : "r"(0x43084308u));
 }
 
+// (a0, a1) *= (b0, b1), one packed multiply
+__device__ __forceinline__ void fmul2x(float &a0, float &a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rb, {%2, %3};\n\t"
+        "mul.rn.f32x2 ra, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 // fp16 scale i (0..7) of eight packed in s
 __device__ __forceinline__ float scale_of(const uint4 &s, int i)
 {
@@ -182,11 +195,18 @@ __device__ __forceinline__ void mma_block(const uint8_t *st, int g, int t, int s
 // each stage's slot, warp `sub` taking its sub-th share of the stage's
 // blocks.  wmap: the repacked rows (8-byte units); smap: the same rows with
 // the q8_0 scales' box.
-template <int WF, int M>
+//
+// q8_1 activations (q4_0 weights): the codes are staged as exact bf16 values
+// and each block's scale d_x in a table; a block's MMA sum is then the exact
+// integer sum_i (q_w - 8) q_x of the integer-dot kernels (|sum| < 2^15, so
+// exact in fp32 whatever the order of the tensor core's additions), and
+// y += (d_w d_x) sum, in their order of rounding.
+template <int WF, int XF, int M>
 __global__ void __launch_bounds__(512, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap, const MmaParams p)
 {
     static_assert(M == 4 || M == 8, "tensor-core GEMV: M = 4 or 8");
+    static_assert(XF == X_BF16 || (XF == X_Q8_1 && WF == W_Q4_0), "tensor-core GEMV: bf16 activations, or q8_1 with q4_0");
     using G = MmaGeom<WF>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_abort;
@@ -256,10 +276,13 @@ __global__ void __launch_bounds__(512, 1)
     // SM's copy queue; each CTA its 1/grid share), into shared memory once
     // the previous grid has completed (it may be their producer)
     if (tid == 32) {
-        const uint32_t xb = (uint32_t)(M * p.K * 2);
+        // the 16-byte-aligned span around X (q8_1 rows are only 4-byte aligned)
+        const uintptr_t xa = reinterpret_cast<uintptr_t>(p.X);
+        const uint32_t xoff = (uint32_t)(xa & 15);
+        const uint32_t xb = (xoff + (uint32_t)((XF == X_BF16) ? M * p.K * 2 : M * nbx * Q8_1_BYTES) + 15) & ~15u;
         const uint32_t ch = ((xb + gridDim.x - 1) / gridDim.x + 15) & ~15u;
         const uint32_t at = blockIdx.x * ch;
-        if (at < xb) prefetch_l2_bulk(p.X + at, min(ch, xb - at));
+        if (at < xb) prefetch_l2_bulk(reinterpret_cast<const uint8_t *>(xa - xoff) + at, min(ch, xb - at));
     }
     if (tid == 0) {
         for (int i = 0; i < NG * D; i++) mbar_init(bar0 + 8 * i, 1);
@@ -287,7 +310,7 @@ __global__ void __launch_bounds__(512, 1)
     // bank conflicts) from its two 8-byte source pieces.  Every CTA reads all
     // of X: each starts at its own offset, so that at any moment the CTAs
     // ask different L2 lines for it.
-    {
+    if constexpr (XF == X_BF16) {
         constexpr int XU = 8;                      // chunks per thread and round
         const int n16 = M * nbx * 4;
         const int rot = (int)(((int64_t)blockIdx.x * 389) % n16);
@@ -316,6 +339,45 @@ __global__ void __launch_bounds__(512, 1)
                 }
             }
         }
+    } else {
+        // q8_1 blocks (36 B: d, s, 32 codes; 4-byte aligned): thread i stages
+        // chunk i, lane c's codes 4c .. 4c + 3 and 16 + 4c .. 16 + 4c + 3 as
+        // exact bf16 values, and the block's d into the scale table
+        constexpr int XU = 8;
+        const int n16 = M * nbx * 4;
+        const int rot = (int)(((int64_t)blockIdx.x * 389) % n16);
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(p.X);     // 9 words per block
+        float *xd = reinterpret_cast<float *>(smem + p.xd_off);
+        for (int i0 = tid; i0 < n16; i0 += XU * (int)blockDim.x) {
+            uint32_t lo[XU], hi[XU], dw[XU];
+#pragma unroll
+            for (int k = 0; k < XU; k++) {
+                int i = i0 + k * (int)blockDim.x + rot;
+                i -= (i >= n16) ? n16 : 0;
+                if (i0 + k * (int)blockDim.x < n16) {
+                    const int blk = i >> 2, c = i & 3;          // rows are contiguous: block blk of X
+                    lo[k] = src[(size_t)blk * 9 + 1 + c];
+                    hi[k] = src[(size_t)blk * 9 + 5 + c];
+                    dw[k] = (c == 0) ? src[(size_t)blk * 9] : 0u;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < XU; k++) {
+                int i = i0 + k * (int)blockDim.x + rot;
+                i -= (i >= n16) ? n16 : 0;
+                if (i0 + k * (int)blockDim.x < n16) {
+                    const int blk = i >> 2, c = i & 3;
+                    const int m = blk / nbx, b = blk - m * nbx;
+                    uint32_t l0, l1, h0, h1;
+                    q8_word_bf16(lo[k], l0, l1);
+                    q8_word_bf16(hi[k], h0, h1);
+                    *reinterpret_cast<uint4 *>(xs + m * p.x_pitch + b * 64 + 16 * c) = make_uint4(l0, l1, h0, h1);
+                    if (c == 0) xd[b * 8 + m] = half_bits_to_float(dw[k] & 0xffffu);
+                }
+            }
+        }
+        for (int i = tid; i < nbx * (8 - M); i += blockDim.x)   // the zero columns' scales
+            xd[(i / (8 - M)) * 8 + M + i % (8 - M)] = 0.f;
     }
     __syncthreads();
 
@@ -354,8 +416,19 @@ __global__ void __launch_bounds__(512, 1)
             auto qblock = [&](int s, float d0, float d8) {
                 float cb[4] = {0.f, 0.f, 0.f, 0.f};
                 mma_block<WF>(st, g, t, s, xload(s), cb);
-                ffma2(c[0], c[1], cb[0], cb[1], d0, d0);
-                ffma2(c[2], c[3], cb[2], cb[3], d8, d8);
+                if constexpr (XF == X_Q8_1) {
+                    // columns 2t, 2t + 1 have their own d_x: (d_w d_x) sum
+                    const float2 dx = *reinterpret_cast<const float2 *>(
+                        reinterpret_cast<const float *>(smem + p.xd_off) + (ts * G::SB + s) * 8 + 2 * t);
+                    float e0 = d0, e1 = d0, e2 = d8, e3 = d8;
+                    fmul2x(e0, e1, dx.x, dx.y);
+                    fmul2x(e2, e3, dx.x, dx.y);
+                    ffma2(c[0], c[1], e0, e1, cb[0], cb[1]);
+                    ffma2(c[2], c[3], e2, e3, cb[2], cb[3]);
+                } else {
+                    ffma2(c[0], c[1], cb[0], cb[1], d0, d0);
+                    ffma2(c[2], c[3], cb[2], cb[3], d8, d8);
+                }
             };
             for (int s8 = s0; s8 < s1; s8 += 8) {
                 const uint4 sc0 = *reinterpret_cast<const uint4 *>(sg + 2 * s8);
@@ -431,13 +504,13 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-template <int WF>
+template <int WF, int XF>
 __host__ cudaError_t gemv_mma_launch(const CUtensorMap &wmap, const CUtensorMap &smap, const MmaParams &p, int M,
                                      dim3 grid, int threads, size_t smem, cudaStream_t stream, bool pdl,
                                      int *occupancy)
 {
     if (M != 4 && M != 8) return cudaErrorInvalidValue;
-    auto kern = (M == 8) ? gemv_mma_kernel<WF, 8> : gemv_mma_kernel<WF, 4>;
+    auto kern = (M == 8) ? gemv_mma_kernel<WF, XF, 8> : gemv_mma_kernel<WF, XF, 4>;
     if (occupancy) {
         cudaError_t e = lpr_allow_smem(kern, smem);
         if (e != cudaSuccess) return e;

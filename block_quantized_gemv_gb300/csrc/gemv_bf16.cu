@@ -18,6 +18,6 @@ int gemv_x_stage_bytes_bf16(int nc, int nb, int bf16) { return bf16 ? x_stage_ro
 cudaError_t gemv_mma_run_bf16(const CUtensorMap &wmap, const CUtensorMap &smap, const MmaParams &p, int M, dim3 grid, int threads, size_t smem,
                             cudaStream_t stream, bool pdl, int *occupancy)
 {
-    return gemv_mma_launch<W_BF16>(wmap, smap, p, M, grid, threads, smem, stream, pdl, occupancy);
+    return gemv_mma_launch<W_BF16, X_BF16>(wmap, smap, p, M, grid, threads, smem, stream, pdl, occupancy);
 }
 }  // namespace bqg

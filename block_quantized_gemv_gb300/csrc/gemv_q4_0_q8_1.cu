@@ -1,5 +1,6 @@
 // gemv_q4_0_q8_1.cu -- instantiations of the skinny-GEMV kernel for W_Q4_0 weights x X_Q8_1 activations.
 #include "bqg_gemv.cuh"
+#include "bqg_gemv_mma.cuh"
 
 namespace bqg {
 // The check instantiation of the q4_0 x q8_1 kernel at M = 1 (every rows-per-
@@ -33,4 +34,9 @@ cudaError_t gemv_lpr_dots_run_q4_0_q8_1(const GemvParams &p, dim3 grid, int thre
     return gemv_lpr_dots_dispatch(p, grid, threads, smem, stream, occupancy);
 }
 int gemv_x_stage_bytes_q4_0_q8_1(int nc, int nb, int) { return x_stage_row_bytes<W_Q4_0, X_Q8_1>(nc, nb); }
+cudaError_t gemv_mma_run_q4_0_q8_1(const CUtensorMap &wmap, const CUtensorMap &smap, const MmaParams &p, int M, dim3 grid,
+                                  int threads, size_t smem, cudaStream_t stream, bool pdl, int *occupancy)
+{
+    return gemv_mma_launch<W_Q4_0, X_Q8_1>(wmap, smap, p, M, grid, threads, smem, stream, pdl, occupancy);
+}
 }  // namespace bqg

@@ -163,7 +163,9 @@ int bqg_gemv_q4_0(const void *Wp, const void *X, float *Y, int M, int64_t N, int
                   void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* q4_0 weights x q8_1 activations (M in {1, 2, 4, 8}).  Per block the
- * integer dot sumi = sum_i (qw_i - 8) * qx_i is exact (int32, dp4a), and
+ * integer dot sumi = sum_i (qw_i - 8) * qx_i is exact (int32 by dp4a; at
+ * M = 8 on the tensor cores, from exact bf16 operands, an fp32 sum of
+ * integers below 2^15 in magnitude, so exact as well), and
  * Y += (d_w * d_x) * sumi in fp32.  Xq: M x K/32 q8_1 blocks. */
 int bqg_gemv_q4_0_q8_1(const void *Wp, const void *Xq, float *Y, int M, int64_t N, int64_t K,
                        void *ws, size_t ws_bytes, cudaStream_t stream);

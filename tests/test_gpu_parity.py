@@ -231,6 +231,14 @@ def test_gemv_tensor_core_route(ora, fmt, M, N, K):
     run_gemv(ora, fmt, BF16, M, N, K, seed=3 * N + K + M)
 
 
+@pytest.mark.parametrize("N,K", TC_SHAPES)
+def test_gemv_q4_0_q8_1_tensor_core_route(ora, N, K):
+    """q4_0 x q8_1 at M = 8 on the tensor cores: each block's MMA sum is the
+    exact integer dot, scaled by d_w d_x."""
+    assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, 8, N, K) == bqg.ROUTE_TENSOR_CORE
+    run_gemv(ora, Q4_0, Q8_1, 8, N, K, seed=5 * N + K)
+
+
 def test_gemv_routes():
     """The route each shape class takes (no launch)."""
     tc, rows = bqg.ROUTE_TENSOR_CORE, bqg.ROUTE_LANES_PER_ROW_ROWS
@@ -240,8 +248,9 @@ def test_gemv_routes():
     # M = 1: the whole-row lanes-per-row kernel on the headline shape
     assert bqg.gemv_route(bqg.OP_GEMV_BF16, 1, 12288, 4096) == rows
     assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, 1, 12288, 4096) == rows
-    # q8_1 activations never take the tensor-core route
-    assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, 8, 14336, 4096) != tc
+    # q8_1 activations: the tensor-core route at M = 8, the integer-dot kernel at M = 4
+    assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, 8, 14336, 4096) == tc
+    assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, 4, 14336, 4096) == rows
     # staged activations above 80 KiB (M = 8, K = 11008): not the tensor-core route
     assert bqg.gemv_route(bqg.OP_GEMV_Q8_0, 8, 4096, 11008) != tc
 
