@@ -255,31 +255,39 @@ def test_gemv_routes():
     assert bqg.gemv_route(bqg.OP_GEMV_Q8_0, 8, 4096, 11008) != tc
 
 
+@pytest.mark.parametrize("M", [1, 8])
 @pytest.mark.parametrize("N,K", [(64, 1024), (1000, 4096), (130, 11008)])
-def test_gemv_q4_0_q8_1_float_is_the_exact_integer_dots_scaled(ora, N, K):
+def test_gemv_q4_0_q8_1_float_is_the_exact_integer_dots_scaled(ora, M, N, K):
     """Each output is sum_b fp32(d_w d_x) * sumi_b with sumi_b the exact
     integer dot: against that sum (fp64, from the oracle's dots and scales)
     the GPU may differ only by fp32 accumulation, |err| <= (nb + 2) 2^-24
     sum_b |fp32(d_w d_x) sumi_b| -- far inside the benchmark spec's bound, so a
-    wrong integer would show."""
+    wrong integer would show.  At M = 1 the integer-dot kernels compute the
+    dots; at M = 8 with K <= 5056 the tensor-core kernel does (exact bf16
+    operands, integer sums below 2^15)."""
     _, canon = make_weights(ora, Q4_0, N, K, seed=5)
-    xq = ora.quantize(Q8_1, synth.rms_normalised_f32(1, K, seed=6))
+    xq = ora.quantize(Q8_1, synth.rms_normalised_f32(M, K, seed=6))
     Wp = gpu_repacked(Q4_0, canon, N, K)
-    Y = nan_like((1, N))
-    bqg.gemv_q4_0_q8_1(Wp, synth.u8_tensor(xq).view(1, -1), N, K, out=Y,
-                       ws=bqg.workspace(bqg.OP_GEMV_Q4_0_Q8_1, 1, N, K))
+    Y = nan_like((M, N))
+    bqg.gemv_q4_0_q8_1(Wp, synth.u8_tensor(xq).view(M, -1), N, K, out=Y,
+                       ws=bqg.workspace(bqg.OP_GEMV_Q4_0_Q8_1, M, N, K))
     torch.cuda.synchronize()
+    if M == 8 and K <= 5056:
+        assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, M, N, K) == bqg.ROUTE_TENSOR_CORE
     nb = K // 32
-    dots = ora.block_dots_q4_0_q8_1(canon, xq, N, K).astype(np.float64)
     dw = canon.reshape(N, nb, 18)[:, :, 0:2].copy().view(np.float16).reshape(N, nb).astype(np.float32)
-    dx = xq.reshape(nb, 36)[:, 0:2].copy().view(np.float16).reshape(nb).astype(np.float32)
-    scale = (dw * dx[None, :]).astype(np.float64)           # the fp32 product, rounded as the kernel rounds it
-    terms = scale * dots
-    want = terms.sum(axis=1)
-    bound = (nb + 2) * 2.0 ** -24 * np.abs(terms).sum(axis=1) + 1e-30
-    y = Y.cpu().double().numpy()[0]
+    y = Y.cpu().double().numpy()
     assert np.all(np.isfinite(y))
-    assert np.all(np.abs(y - want) <= bound), f"max err/bound {np.max(np.abs(y - want) / bound):.3g}"
+    xrows = np.asarray(xq).reshape(M, nb * 36)
+    for m in range(M):
+        xm = np.ascontiguousarray(xrows[m])
+        dots = ora.block_dots_q4_0_q8_1(canon, xm, N, K).astype(np.float64)
+        dx = xm.reshape(nb, 36)[:, 0:2].copy().view(np.float16).reshape(nb).astype(np.float32)
+        scale = (dw * dx[None, :]).astype(np.float64)       # the fp32 product, rounded as the kernel rounds it
+        terms = scale * dots
+        want = terms.sum(axis=1)
+        bound = (nb + 2) * 2.0 ** -24 * np.abs(terms).sum(axis=1) + 1e-30
+        assert np.all(np.abs(y[m] - want) <= bound), f"row {m}: max err/bound {np.max(np.abs(y[m] - want) / bound):.3g}"
 
 
 @pytest.mark.parametrize("fmt,xf", [(BF16, BF16), (Q8_0, BF16), (Q4_0, Q8_1), (Q4_0, BF16)])
