@@ -539,8 +539,8 @@ int check_k(int64_t K)
     return BQG_OK;
 }
 
-// The tensor-core route (bqg_gemv_mma.cuh): M = 4 or 8, bf16 activations,
-// one matrix, outputs stored as they are, staged activations within 80 KiB
+// The tensor-core route (bqg_gemv_mma.cuh): M = 4 or 8, bf16 activations
+// (and q4_0 x bf16 at M = 2, q4_0 x q8_1 at M = 8), one matrix, outputs stored as they are, staged activations within 80 KiB
 // (M K <= about 40960).  One CTA per SM, eight warps; as many slots per warp
 // (at most four) as the shared memory left by the staged activation rows
 // and the partial records holds.  Measured on the sweep shape (K = 4096,
@@ -569,7 +569,10 @@ int plan_mma(int wf, int xf, int M, int64_t N, int64_t K, const DevInfo &dev, in
     static const int force_D = env_int("BQG_MMA_D", 0);
     static const int force_nw = env_int("BQG_MMA_WARPS", 0);
     static const int force_gw = env_int("BQG_MMA_GROUP", 0);
-    if (off || (M != 4 && M != 8) || N <= 0) return BQG_ERR_UNSUPPORTED_SHAPE;
+    if (off || N <= 0) return BQG_ERR_UNSUPPORTED_SHAPE;
+    // M = 2: q4_0 x bf16 only (its lanes-per-row dot is bound by the
+    // conversion; measured 13.70 -> 12.28 us at N = 14336, 6.18 -> 5.83 at 4096)
+    if (M != 4 && M != 8 && !(M == 2 && wf == W_Q4_0 && xf == X_BF16)) return BQG_ERR_UNSUPPORTED_SHAPE;
     // q8_1 activations (q4_0 weights): at M = 8, where the integer-dot
     // lanes-per-row kernel is bound by its dots (at M = 4 it is faster)
     if (xf == X_Q8_1 && (wf != W_Q4_0 || M != 8)) return BQG_ERR_UNSUPPORTED_SHAPE;
@@ -687,7 +690,7 @@ int gemv_plain(int wf, int xf, int fmt, const void *Wp, const void *X, float *Y,
     if (int st = check_k(K)) return st;
     if (wf == W_BF16 && K > 16384) return BQG_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(Wp) || !aligned16(Y) || !aligned(X, xf == X_Q8_1 ? 4 : 16)) return BQG_ERR_MISALIGNED;
-    if ((M == 4 || M == 8) && N > 0) {
+    if ((M == 2 || M == 4 || M == 8) && N > 0) {
         const int st = run_mma(wf, xf, fmt, Wp, X, Y, M, N, K, stream);
         if (st != BQG_ERR_UNSUPPORTED_SHAPE) return st;
     }
@@ -1097,7 +1100,7 @@ int bqg_gemv_route(int op, int M, int64_t N, int64_t K, int *route)
     int st = current_device(&dev);
     if (st) return st;
     cudaGetDevice(&dv);
-    if (M == 4 || M == 8) {
+    if (M == 2 || M == 4 || M == 8) {
         MmaPlan mp;
         st = plan_mma(wf, xf, M, N, K, dev, dv, &mp);
         if (st == BQG_OK) {

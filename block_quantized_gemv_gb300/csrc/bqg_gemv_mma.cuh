@@ -205,7 +205,7 @@ template <int WF, int XF, int M>
 __global__ void __launch_bounds__(512, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap, const MmaParams p)
 {
-    static_assert(M == 4 || M == 8, "tensor-core GEMV: M = 4 or 8");
+    static_assert(M == 2 || M == 4 || M == 8, "tensor-core GEMV: M = 2, 4 or 8");
     static_assert(XF == X_BF16 || (XF == X_Q8_1 && WF == W_Q4_0), "tensor-core GEMV: bf16 activations, or q8_1 with q4_0");
     using G = MmaGeom<WF>;
     extern __shared__ uint8_t smem_raw[];
@@ -509,8 +509,13 @@ __host__ cudaError_t gemv_mma_launch(const CUtensorMap &wmap, const CUtensorMap 
                                      dim3 grid, int threads, size_t smem, cudaStream_t stream, bool pdl,
                                      int *occupancy)
 {
-    if (M != 4 && M != 8) return cudaErrorInvalidValue;
+    if (M != 2 && M != 4 && M != 8) return cudaErrorInvalidValue;
     auto kern = (M == 8) ? gemv_mma_kernel<WF, XF, 8> : gemv_mma_kernel<WF, XF, 4>;
+    if constexpr (WF == W_Q4_0 && XF == X_BF16) {        // M = 2: q4_0 x bf16 only
+        if (M == 2) kern = gemv_mma_kernel<WF, XF, 2>;
+    } else {
+        if (M == 2) return cudaErrorInvalidValue;
+    }
     if (occupancy) {
         cudaError_t e = lpr_allow_smem(kern, smem);
         if (e != cudaSuccess) return e;

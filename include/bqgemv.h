@@ -143,8 +143,9 @@ int bqg_rmsnorm_quantize_q8_1(const void *x, int x_dtype, const float *gamma, fl
  * needs no initialisation and must not be shared by calls that overlap.
  * fp32 accumulation.  At M = 1 and 2 (and where the route below does not
  * apply) bqg_gemv_q8_0/q4_0 dequantize (q*d, (q-8)*d) exactly and add the
- * products in fp32.  At M = 4 and 8 (staged activations M*K*2 bytes within
- * 80 KiB; bf16 weights with N >= 16 * 76) the products go to the tensor
+ * products in fp32.  At M = 4 and 8 (and for q4_0 at M = 2; staged
+ * activations M*K*2 bytes within 80 KiB; bf16 weights with N >= 16 * 76)
+ * the products go to the tensor
  * cores (mma.sync, bf16 operands: q8_0 codes, q4_0 values q-8 and bf16
  * weights are exact in bf16, each product exact in fp32); each block's sum
  * over its 32 values is then scaled by its d in fp32, and bf16 weights
@@ -321,7 +322,8 @@ enum {
     BQG_ROUTE_K_SLICE = 0,                /* K-slice kernel (staged activations too large) */
     BQG_ROUTE_LANES_PER_ROW = 1,          /* lanes-per-row kernel, general form (split K) */
     BQG_ROUTE_LANES_PER_ROW_ROWS = 2,     /* lanes-per-row kernel, whole rows per stage */
-    BQG_ROUTE_TENSOR_CORE = 3             /* tensor-core kernel (M = 4, 8; bf16 activations) */
+    BQG_ROUTE_TENSOR_CORE = 3             /* tensor-core kernel (M = 4, 8 with bf16 activations, q4_0 x bf16 at M = 2,
+                                             q4_0 x q8_1 at M = 8) */
 };
 int bqg_gemv_route(int op, int M, int64_t N, int64_t K, int *route);
 

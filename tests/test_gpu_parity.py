@@ -245,6 +245,9 @@ def test_gemv_routes():
     assert bqg.gemv_route(bqg.OP_GEMV_Q8_0, 8, 14336, 4096) == tc
     assert bqg.gemv_route(bqg.OP_GEMV_BF16, 4, 14336, 4096) == tc
     assert bqg.gemv_route(bqg.OP_GEMV_Q4_0, 4, 14336, 4096) == tc
+    # M = 2: q4_0 x bf16 on the tensor cores, the other formats on the lanes-per-row kernel
+    assert bqg.gemv_route(bqg.OP_GEMV_Q4_0, 2, 14336, 4096) == tc
+    assert bqg.gemv_route(bqg.OP_GEMV_Q8_0, 2, 14336, 4096) == rows
     # M = 1: the whole-row lanes-per-row kernel on the headline shape
     assert bqg.gemv_route(bqg.OP_GEMV_BF16, 1, 12288, 4096) == rows
     assert bqg.gemv_route(bqg.OP_GEMV_Q4_0_Q8_1, 1, 12288, 4096) == rows
