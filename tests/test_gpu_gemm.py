@@ -78,6 +78,19 @@ def test_gemm_small(ora, M, N, K, fmt):
 
 
 @pytest.mark.parametrize("fmt", [Q4_0, Q8_0])
+@pytest.mark.parametrize("M,N,K", [(256, 10240, 1024), (640, 5120, 2048)])
+def test_gemm_big_units(ora, M, N, K, fmt):
+    """Shapes whose order keeps units of 256 activation rows whole on a
+    152-SM part (more than half the CTAs take one): every unit big (M = 256),
+    and big units followed by single-tile units (M / 128 odd).  Sampled rows
+    cover both 128-row halves of every big unit and the single tile."""
+    rng = np.random.default_rng(M + N)
+    cols = np.unique(np.concatenate([rng.choice(N, 64, replace=False), [0, 127, 128, N - 1]]))
+    rows = np.unique(np.concatenate([rng.choice(M, 48, replace=False), [0, 127, 128, 255, M - 128, M - 1]]))
+    run_gemm(ora, M, N, K, seed=M + K, rows=rows, cols=cols, fmt=fmt)
+
+
+@pytest.mark.parametrize("fmt", [Q4_0, Q8_0])
 def test_gemm_one_dominant_term(ora, fmt):
     """Short K with one activation per row far larger than the rest: the sum is
     one product, so a single bf16 rounding of that weight (up to 2^-9 of it)
