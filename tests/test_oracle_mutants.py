@@ -36,6 +36,29 @@ MUTANTS = [
     ("rmsnorm_sum_not_mean", "sqrt(s / (double)K + (double)eps)", "sqrt(s + (double)eps)"),
     ("rmsnorm_eps_outside_root", "sqrt(s / (double)K + (double)eps)", "sqrt(s / (double)K) + (double)eps"),
     ("rmsnorm_gamma_ignored", "if (gamma) v = v * gamma[k];", "if (gamma) v = v;"),
+    ("q8_0_scale_over_128", "amax / 127.0f);\n    float d = fp16_to_float(dh);\n    wr_u16(blk, dh);",
+     "amax / 128.0f);\n    float d = fp16_to_float(dh);\n    wr_u16(blk, dh);"),
+    ("q8_1_scale_over_128", "amax / 127.0f);\n    float d = fp16_to_float(dh);\n    int sum = 0;",
+     "amax / 128.0f);\n    float d = fp16_to_float(dh);\n    int sum = 0;"),
+    ("q8_0_codes_read_unsigned", "out[b * QK + i] = (double)(int8_t)blk[2 + i] * d;",
+     "out[b * QK + i] = (double)blk[2 + i] * d;"),
+    ("q8_0_dequant_unscaled", "out[b * QK + i] = (double)(int8_t)blk[2 + i] * d;",
+     "out[b * QK + i] = (double)(int8_t)blk[2 + i];"),
+    ("q8_1_dequant_uses_s", "double d = ref_fp16_to_double(rd_u16(blk));\n            for (int i = 0; i < QK; i++) out[b * QK + i] = (double)(int8_t)blk[4 + i] * d;",
+     "double d = ref_fp16_to_double(rd_u16(blk + 2));\n            for (int i = 0; i < QK; i++) out[b * QK + i] = (double)(int8_t)blk[4 + i] * d;"),
+    ("q4_0_clamp_at_16", "clampf(roundf(x[i] / d) + 8.0f, 0.0f, 15.0f)", "clampf(roundf(x[i] / d) + 8.0f, 0.0f, 16.0f)"),
+    ("block_dots_x_unsigned", "s += (int64_t)(lo - 8) * (int8_t)xb[4 + j];", "s += (int64_t)(lo - 8) * xb[4 + j];"),
+    ("block_dots_high_nibble_wrong_x", "s += (int64_t)(hi - 8) * (int8_t)xb[4 + j + 16];",
+     "s += (int64_t)(hi - 8) * (int8_t)xb[4 + j];"),
+    ("repack_q8_0_halves_swapped", "memcpy(tile + 16 * s, blk + 2, 16);\n                memcpy(tile + 512 + 16 * s, blk + 18, 16);",
+     "memcpy(tile + 16 * s, blk + 18, 16);\n                memcpy(tile + 512 + 16 * s, blk + 2, 16);"),
+    ("repack_q8_0_scale_stride", "memcpy(tile + 1024 + 2 * s, blk, 2);", "memcpy(tile + 1024 + s, blk, 2);"),
+    ("repack_row_stride_dropped",
+     "uint8_t *tile = packed + (n * T + b / 32) * tb;\n            int64_t s = b % 32;\n            if (fmt == FMT_Q4_0) {\n                const uint8_t",
+     "uint8_t *tile = packed + (n + b / 32) * tb;\n            int64_t s = b % 32;\n            if (fmt == FMT_Q4_0) {\n                const uint8_t"),
+    ("swiglu_u_dropped", "h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(-g[i]));"),
+    ("fp16_overflow_threshold", "if (a >= 65520.0)", "if (a > 65504.0)"),
+    ("fp16_subnormal_exponent", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
 ]
 
 
