@@ -59,6 +59,9 @@ MUTANTS = [
     ("swiglu_u_dropped", "h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(-g[i]));"),
     ("fp16_overflow_threshold", "if (a >= 65520.0)", "if (a > 65504.0)"),
     ("fp16_subnormal_exponent", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    ("fp16_ties_away", "double n = nearbyint(ldexp(a, -ulp_exp));", "double n = round(ldexp(a, -ulp_exp));"),
+    ("gemv_k_shifted", "s += w[k] * x[k];", "s += w[k] * x[(k + 1) % K];"),
+    ("rmsnorm_divides", "float v = xr[k] * rr;", "float v = xr[k] / rr;"),
 ]
 
 
