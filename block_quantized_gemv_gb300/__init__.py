@@ -25,6 +25,7 @@ OP_QKV_Q4_0_Q8_1, OP_GATE_UP_Q4_0_Q8_1, OP_GEMM_Q4_0_BF16 = 4, 5, 6
 OP_GATE_UP_Q8_1_Q4_0_Q8_1, OP_GEMM_Q8_0_BF16, OP_DECODE_LAYER_Q4_0_Q8_1 = 7, 8, 9
 BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q8_1: 36}
 QK = 32
+TILE_BYTES = {Q8_0: 1088, Q4_0: 576}     # 32 blocks of one repacked row
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libbqgemv.so")
@@ -135,17 +136,36 @@ def check_device(index: int, current: int, name: str) -> None:
                          f"call under torch.cuda.device({index})")
 
 
-def _dev(t: torch.Tensor, name: str, dtype=None, numel=None):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
-    check_device(t.device.index, _current_device(), name)
+def _check_tensor(t: torch.Tensor, name: str, dtype=None, numel=None) -> None:
+    """Layout, dtype and size checks shared by device and host operands:
+    `numel` is the byte count the call will touch."""
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if numel is not None and t.nbytes < numel:
         raise ValueError(f"{name} holds {t.nbytes} bytes, needs {numel}")
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, numel=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    check_device(t.device.index, _current_device(), name)
+    _check_tensor(t, name, dtype, numel)
     return t.data_ptr()
+
+
+def weight_bytes(fmt: int, N: int, K: int):
+    """Bytes of N repacked weight rows of K values (the layout of
+    include/bqgemv.h: bf16 row-major; q4_0 / q8_0 rows of ceil(K/32/32)
+    tiles of 576 / 1088 bytes), or None for a shape the library refuses by
+    itself (K not a positive multiple of 32, N < 1).  The C boundary takes
+    the weights as a bare pointer, so the binding checks their size."""
+    if N < 1 or K < 1 or K % QK:
+        return None
+    if fmt == BF16:
+        return N * K * 2
+    return N * ((K // QK + 31) // 32) * TILE_BYTES[fmt]
 
 
 def host_alias(t: torch.Tensor) -> int:
@@ -163,10 +183,7 @@ def host_alias(t: torch.Tensor) -> int:
 def _dev_or_host(t: torch.Tensor, name: str, dtype=None, numel=None):
     """_dev for a CUDA tensor; the host alias for a pinned CPU tensor."""
     if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
-        if dtype is not None and t.dtype != dtype:
-            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-        if numel is not None and t.nbytes < numel:
-            raise ValueError(f"{name} holds {t.nbytes} bytes, needs {numel}")
+        _check_tensor(t, name, dtype, numel)
         return host_alias(t)
     return _dev(t, name, dtype, numel)
 
@@ -249,31 +266,31 @@ def rmsnorm_quantize_q8_1(x: torch.Tensor, gamma: torch.Tensor | None = None, ep
     return out
 
 
-def _gemv(fn: str, Wp, X, N: int, K: int, M: int, out, ws, stream, xbytes):
+def _gemv(fn: str, wfmt: int, Wp, X, N: int, K: int, M: int, out, ws, stream, xbytes):
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=X.device)
     wsp, wsb = _ws(ws)
-    _check(getattr(load(), fn)(_dev(Wp, "Wp"), _dev(X, "X", numel=xbytes),
+    _check(getattr(load(), fn)(_dev(Wp, "Wp", numel=weight_bytes(wfmt, N, K)), _dev(X, "X", numel=xbytes),
                                _dev_or_host(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)),
            fn)
     return out
 
 
 def gemv_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
-    return _gemv("bqg_gemv_bf16", Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
+    return _gemv("bqg_gemv_bf16", BF16, Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
 
 
 def gemv_q8_0(Wp, X, N, K, out=None, ws=None, stream=None):
-    return _gemv("bqg_gemv_q8_0", Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
+    return _gemv("bqg_gemv_q8_0", Q8_0, Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
 
 
 def gemv_q4_0(Wp, X, N, K, out=None, ws=None, stream=None):
-    return _gemv("bqg_gemv_q4_0", Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
+    return _gemv("bqg_gemv_q4_0", Q4_0, Wp, X, N, K, X.shape[0], out, ws, stream, X.shape[0] * K * 2)
 
 
 def gemv_q4_0_q8_1(Wp, Xq, N, K, out=None, ws=None, stream=None):
     M = Xq.shape[0]
-    return _gemv("bqg_gemv_q4_0_q8_1", Wp, Xq, N, K, M, out, ws, stream, M * row_bytes(Q8_1, K))
+    return _gemv("bqg_gemv_q4_0_q8_1", Q4_0, Wp, Xq, N, K, M, out, ws, stream, M * row_bytes(Q8_1, K))
 
 
 def gemv_q4_0_q8_1_noalloc(Wp, Xq, N, K, out=None, stream=None):
@@ -282,7 +299,7 @@ def gemv_q4_0_q8_1_noalloc(Wp, Xq, N, K, out=None, stream=None):
     M = Xq.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=Xq.device)
-    _check(load().bqg_gemv_q4_0_q8_1_noalloc(_dev(Wp, "Wp"), _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
+    _check(load().bqg_gemv_q4_0_q8_1_noalloc(_dev(Wp, "Wp", numel=weight_bytes(Q4_0, N, K)), _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
                                              _dev_or_host(out, "Y", torch.float32, M * N * 4), M, N, K,
                                              _stream(stream)), "bqg_gemv_q4_0_q8_1_noalloc")
     return out
@@ -297,7 +314,9 @@ def gemv_q4_0_q8_1_qkv(Wq, Wk, Wv, Xq, Nq, Nkv, K, out=None, ws=None, stream=Non
                torch.empty((M, Nkv), dtype=torch.float32, device=dev))
     Yq, Yk, Yv = out
     wsp, wsb = _ws(ws)
-    _check(load().bqg_gemv_q4_0_q8_1_qkv(_dev(Wq, "Wq"), _dev(Wk, "Wk"), _dev(Wv, "Wv"),
+    _check(load().bqg_gemv_q4_0_q8_1_qkv(_dev(Wq, "Wq", numel=weight_bytes(Q4_0, Nq, K)),
+                                         _dev(Wk, "Wk", numel=weight_bytes(Q4_0, Nkv, K)),
+                                         _dev(Wv, "Wv", numel=weight_bytes(Q4_0, Nkv, K)),
                                          _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
                                          _dev(Yq, "Yq", torch.float32, M * Nq * 4),
                                          _dev(Yk, "Yk", torch.float32, M * Nkv * 4),
@@ -311,7 +330,8 @@ def gemv_q4_0_q8_1_gate_up_swiglu(Wg, Wu, Xq, N, K, out=None, ws=None, stream=No
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=Xq.device)
     wsp, wsb = _ws(ws)
-    _check(load().bqg_gemv_q4_0_q8_1_gate_up_swiglu(_dev(Wg, "Wg"), _dev(Wu, "Wu"),
+    _check(load().bqg_gemv_q4_0_q8_1_gate_up_swiglu(_dev(Wg, "Wg", numel=weight_bytes(Q4_0, N, K)),
+                                                    _dev(Wu, "Wu", numel=weight_bytes(Q4_0, N, K)),
                                                     _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
                                                     _dev(out, "H", torch.float32, M * N * 4), M, N, K, wsp, wsb,
                                                     _stream(stream)), "bqg_gemv_q4_0_q8_1_gate_up_swiglu")
@@ -325,7 +345,8 @@ def gemv_q4_0_q8_1_gate_up_swiglu_q8_1(Wg, Wu, Xq, N, K, out=None, ws=None, stre
     if out is None:
         out = torch.empty((M, row_bytes(Q8_1, N)), dtype=torch.uint8, device=Xq.device)
     wsp, wsb = _ws(ws)
-    _check(load().bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(_dev(Wg, "Wg"), _dev(Wu, "Wu"),
+    _check(load().bqg_gemv_q4_0_q8_1_gate_up_swiglu_q8_1(_dev(Wg, "Wg", numel=weight_bytes(Q4_0, N, K)),
+                                                         _dev(Wu, "Wu", numel=weight_bytes(Q4_0, N, K)),
                                                          _dev(Xq, "Xq", numel=M * row_bytes(Q8_1, K)),
                                                          _dev(out, "Hq", numel=M * row_bytes(Q8_1, N)), M, N, K,
                                                          wsp, wsb, _stream(stream)),
@@ -349,8 +370,12 @@ def decode_layer_q4_0_q8_1(xa, xb, Wq, Wk, Wv, Wg, Wu, Wd, Nq, Nkv, Nff, K, out=
     Yq, Yk, Yv, Y = out
     wsp, wsb = _ws(ws)
     _check(load().bqg_decode_layer_q4_0_q8_1(_dev(xa, "xa", numel=nx), _dev(xb, "xb", numel=nx), dt,
-                                             _dev(Wq, "Wq"), _dev(Wk, "Wk"), _dev(Wv, "Wv"), _dev(Wg, "Wg"),
-                                             _dev(Wu, "Wu"), _dev(Wd, "Wd"),
+                                             _dev(Wq, "Wq", numel=weight_bytes(Q4_0, Nq, K)),
+                                             _dev(Wk, "Wk", numel=weight_bytes(Q4_0, Nkv, K)),
+                                             _dev(Wv, "Wv", numel=weight_bytes(Q4_0, Nkv, K)),
+                                             _dev(Wg, "Wg", numel=weight_bytes(Q4_0, Nff, K)),
+                                             _dev(Wu, "Wu", numel=weight_bytes(Q4_0, Nff, K)),
+                                             _dev(Wd, "Wd", numel=weight_bytes(Q4_0, K, Nff)),
                                              _dev(Yq, "Yq", torch.float32, Nq * 4), _dev(Yk, "Yk", torch.float32, Nkv * 4),
                                              _dev(Yv, "Yv", torch.float32, Nkv * 4), _dev(Y, "Y", torch.float32, K * 4),
                                              1, Nq, Nkv, Nff, K, wsp, wsb, _stream(stream)),
@@ -370,7 +395,7 @@ def gemm_q4_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=X.device)
     wsp, wsb = _ws(ws)
-    _check(load().bqg_gemm_q4_0_bf16(_dev(Wp, "Wp"), _dev(X, "X", torch.bfloat16, M * K * 2),
+    _check(load().bqg_gemm_q4_0_bf16(_dev(Wp, "Wp", numel=weight_bytes(Q4_0, N, K)), _dev(X, "X", torch.bfloat16, M * K * 2),
                                      _dev(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)),
            "bqg_gemm_q4_0_bf16")
     return out
@@ -381,7 +406,7 @@ def gemm_q8_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=X.device)
     wsp, wsb = _ws(ws)
-    _check(load().bqg_gemm_q8_0_bf16(_dev(Wp, "Wp"), _dev(X, "X", torch.bfloat16, M * K * 2),
+    _check(load().bqg_gemm_q8_0_bf16(_dev(Wp, "Wp", numel=weight_bytes(Q8_0, N, K)), _dev(X, "X", torch.bfloat16, M * K * 2),
                                      _dev(out, "Y", torch.float32, M * N * 4), M, N, K, wsp, wsb, _stream(stream)),
            "bqg_gemm_q8_0_bf16")
     return out
@@ -390,7 +415,7 @@ def gemm_q8_0_bf16(Wp, X, N, K, out=None, ws=None, stream=None):
 def _block_dots(fn, Wp, Xq, N, K, out, stream):
     if out is None:
         out = torch.empty((N, K // QK), dtype=torch.int32, device=Xq.device)
-    _check(getattr(load(), fn)(_dev(Wp, "Wp"), _dev(Xq, "Xq", numel=row_bytes(Q8_1, K)),
+    _check(getattr(load(), fn)(_dev(Wp, "Wp", numel=weight_bytes(Q4_0, N, K)), _dev(Xq, "Xq", numel=row_bytes(Q8_1, K)),
                                _dev(out, "dots", torch.int32, N * (K // QK) * 4), N, K, _stream(stream)), fn)
     return out
 

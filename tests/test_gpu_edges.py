@@ -36,9 +36,12 @@ def test_gemv_at_the_largest_k(ora, fmt, xf, K, M):
     run_gemv(ora, fmt, xf, M, 40, K, seed=K + M)
 
 
-@pytest.mark.parametrize("fn,K", [("gemv_q8_0", 65536 + 32), ("gemv_q4_0", 65536 + 32), ("gemv_bf16", 16384 + 32)])
-def test_gemv_refuses_k_beyond_the_largest(fn, K):
-    Wp = torch.zeros(64, dtype=torch.uint8, device="cuda")
+@pytest.mark.parametrize("fn,fmt,K", [("gemv_q8_0", Q8_0, 65536 + 32), ("gemv_q4_0", Q4_0, 65536 + 32),
+                                      ("gemv_bf16", BF16, 16384 + 32)])
+def test_gemv_refuses_k_beyond_the_largest(fn, fmt, K):
+    # weights of the full repacked size, so that the binding's size check
+    # passes and the library's own shape check is what refuses
+    Wp = torch.zeros(bqg.repacked_size(fmt, 8, K), dtype=torch.uint8, device="cuda")
     X = torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(bqg.BqgError) as e:
         getattr(bqg, fn)(Wp, X, 8, K, out=torch.zeros((1, 8), device="cuda"))
@@ -92,6 +95,21 @@ def test_gemv_degenerate_blocks_and_a_zero_row(ora, fmt, xf, M):
     y = Y.cpu()
     assert not y[1].any(), "an all-zero activation row must give exact zeros"
     assert not y[:, 0].any() and not y[:, 1].any(), "rows with zero scales must give exact zeros"
+
+
+def test_weights_smaller_than_their_layout_are_refused_before_launch():
+    """The C boundary takes the weights as a bare pointer; the binding checks
+    them against the repacked size of the call's shape and refuses a tensor
+    that is too small (ValueError) before anything is enqueued."""
+    N, K = 64, 256
+    W = torch.zeros(bqg.repacked_size(bqg.Q4_0, N, K) - 16, dtype=torch.uint8, device="cuda")
+    X = torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
+    Y = torch.full((1, N), 7.0, device="cuda")
+    torch.cuda.synchronize()
+    with pytest.raises(ValueError, match="Wp holds"):
+        bqg.gemv_q4_0(W, X, N, K, out=Y)
+    torch.cuda.synchronize()
+    assert torch.all(Y == 7.0)          # nothing ran
 
 
 def test_tensor_on_another_device_is_refused_before_launch(monkeypatch):

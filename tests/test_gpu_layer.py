@@ -101,10 +101,15 @@ def test_decode_layer_c3_shape_matches_the_separate_entries(ora):
 def test_decode_layer_rejects_small_workspace():
     K, Nq, Nff = 1024, 256, 512
     z = torch.zeros(1, dtype=torch.uint8, device="cuda")
+
+    def w(n, k):           # zero weights of the repacked size (the binding checks it)
+        return torch.zeros(bqg.repacked_size(bqg.Q4_0, n, k), dtype=torch.uint8, device="cuda")
+
     with pytest.raises(bqg.BqgError) as e:
         bqg.decode_layer_q4_0_q8_1(torch.zeros((1, K), dtype=torch.bfloat16, device="cuda"),
                                    torch.zeros((1, K), dtype=torch.bfloat16, device="cuda"),
-                                   *[z] * 6, Nq, Nq, Nff, K, ws=z)
+                                   w(Nq, K), w(Nq, K), w(Nq, K), w(Nff, K), w(Nff, K), w(K, Nff),
+                                   Nq, Nq, Nff, K, ws=z)
     assert e.value.status == 7
 
 
