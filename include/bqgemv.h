@@ -272,7 +272,11 @@ int bqg_decode_layer_q4_0_q8_1(const void *xa, const void *xb, int x_dtype, cons
  * that rounding could exceed the library's parity bound 1e-3 * sum|w x|,
  * each weight is written exactly as a sum of two bf16 terms, one MMA each.
  * Wp: repacked q4_0 N x K; X: M x K bf16; Y: M x N fp32.
- * M a positive multiple of 128, N a multiple of 128, K a multiple of 64. */
+ * M a positive multiple of 128, N a multiple of 128, K a multiple of 64.
+ * The kernel's shared-memory limit is raised once per process, on the
+ * device current at the first call of each weight format and K range: a
+ * process that calls the GEMM on a second device gets BQG_ERR_CUDA there
+ * (nothing is launched). */
 int bqg_gemm_q4_0_bf16(const void *Wp, const void *X, float *Y, int M, int64_t N, int64_t K,
                        void *ws, size_t ws_bytes, cudaStream_t stream);
 
